@@ -1,0 +1,463 @@
+#!/usr/bin/env python3
+"""Throughput of the BeaconKV eviction step on GB300, one JSON line on stdout.
+
+A step is one eviction period of the whole hot path for every layer and
+sequence of the workload: one bkv_evict (RoPE table, fused score + keep-set
+selection, in-place K/V compaction, FPS of beacons + recents) followed by the
+period's bkv_append_queries calls (one per decode step). The metric is
+evictions per second, one eviction being one (layer, sequence) pair.
+
+Default workload: Qwen3-4B head shape (36 layers, 32 query / 8 KV heads,
+d = 128), batch 192, budget 2048, period 16, prefix 4, recent 16, FPS 32 -> 16.
+Its K/V cache (58 GB) is larger than L2, so no flush is needed between steps.
+Inputs are synthetic and seeded (synth/).
+
+--impl reference times the CPU oracle (oracle/) on this host's cores on a
+bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def aggregate(per_rank_evictions: int, elapsed_s_max: float, world: int) -> float:
+    """Whole-job evictions/s: every rank processes its own full workload (weak scaling)."""
+    return per_rank_evictions * world / elapsed_s_max
+
+
+# ----------------------------------------------------------------------------- byte model
+
+def kernel_bytes(w, R: int, rows_moved_per_launch: float, heads_total: int, n_fps: int) -> dict:
+    """Algorithmic DRAM bytes each launch must move (inputs read once, outputs written once)."""
+    L = w.max_cache
+    units = w.units
+    row = w.d * 2
+    return {
+        "score_select": units * (L * row + R * row + w.budget * 4),
+        "compact": 4 * row * rows_moved_per_launch + units * w.budget * 4,
+        "fps": heads_total * (n_fps * row + w.fps_keep * (row + 1)),
+        "append": heads_total * 2 * row,
+        "rope": 0,
+    }
+
+
+def path_bytes(w, R: int, rows_moved_per_eviction: float, heads_total: int) -> float:
+    """Bytes of one whole period, counting K once (the minimum the method needs):
+    K read, observation rows read, kept written, moved rows (V read, K and V
+    written), new beacons written, one query row per head and step."""
+    row = w.d * 2
+    units = w.units
+    return (units * (w.max_cache * row + R * row + w.budget * 4) + 3 * row * rows_moved_per_eviction
+            + heads_total * w.fps_keep * row + w.period * heads_total * 2 * row)
+
+
+# ----------------------------------------------------------------------------- oracle legs
+
+def _oracle_job(args):
+    """One unit's eviction on the CPU oracle from a seeded steady state; returns seconds."""
+    import numpy as np
+    from oracle import UnitOracle
+    (seed, G, d, theta, budget, prefix, recent, fps_cap, fps_keep, L, period) = args
+    rng = np.random.default_rng(seed)
+
+    def bf16(x):
+        b = x.astype(np.float32).view(np.uint32)
+        b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+        return b.astype(np.uint16)
+
+    n_rq = fps_cap - fps_keep
+    t = 4 * L + 1000
+    uo = UnitOracle(G, d, theta, budget, prefix, recent, fps_cap, fps_keep)
+    qs = lambda n: bf16(rng.standard_normal((n, d)) / math.sqrt(d))
+    uo.load_state([qs(fps_keep) for _ in range(G)], [qs(min(period, n_rq)) for _ in range(G)],
+                  list(range(t - min(period, n_rq) + 1, t + 1)),
+                  bf16(rng.standard_normal((L, d))), bf16(rng.standard_normal((L, d))),
+                  list(range(t - L + 1, t + 1)))
+    t0 = time.perf_counter()
+    uo.evict(t)
+    return time.perf_counter() - t0
+
+
+def oracle_pool():
+    """A spawn-context process pool over every host core, one BLAS thread each."""
+    import multiprocessing as mp
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+    cores = len(os.sched_getaffinity(0))
+    return mp.get_context("spawn").Pool(cores), cores
+
+
+def oracle_rate(w, n_units: int, pool, cores: int, seed: int = 1234):
+    """Evictions/s of the CPU oracle on n_units sampled units, all host cores."""
+    jobs = [(seed + i, w.group, w.d, w.theta, w.budget, w.prefix, w.recent, w.fps_cap, w.fps_keep,
+             w.max_cache, w.period) for i in range(n_units)]
+    t0 = time.perf_counter()
+    times = pool.map(_oracle_job, jobs, chunksize=1)
+    wall = time.perf_counter() - t0
+    return {"value": n_units / wall / w.kv_heads, "cores": cores, "wall_s": wall,
+            "cpu_s": sum(times), "units": n_units}
+
+
+def run_reference(args, w):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    steps, warm = args.steps, args.warmup
+    per_step = args.ref_units_per_step
+    pool, cores = oracle_pool()
+    with pool:
+        for i in range(warm):
+            oracle_rate(w, per_step, pool, cores, seed=10_000 * (i + 1))
+        t0 = time.perf_counter()
+        for i in range(steps):
+            oracle_rate(w, per_step, pool, cores, seed=20_000 + 1000 * i)
+        elapsed = time.perf_counter() - t0
+    value = steps * per_step / w.kv_heads / elapsed
+    out = {
+        "impl": "reference", "metric": "KV evictions/s (all layers x batch)", "value": value,
+        "unit": "evictions/s", "n_gpus": world, "steps": steps, "warmup": warm,
+        "ms_per_step": 1e3 * elapsed / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "layers": w.layers, "batch": w.batch, "heads": w.heads,
+                   "kv_heads": w.kv_heads, "budget": w.budget, "period": w.period},
+        "cpu_baseline": {"value": value, "unit": "evictions/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} steady-state units per step (one eviction = "
+                                   f"{w.kv_heads} units), fp64 oracle, one unit per process"},
+        "e2e": {"value": value, "unit": "evictions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU leg
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    from kv_cache_eviction_head_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        dist.barrier()
+    from kv_cache_eviction_head_gb300 import bkv
+    from synth import SyntheticStream
+
+    stream = SyntheticStream(w, seed=0xBEAC0 + 2, device=dev)
+    K = [torch.empty(w.batch, w.kv_heads, w.max_cache, w.d, dtype=torch.bfloat16, device=dev)
+         for _ in range(w.layers)]
+    V = [torch.empty_like(K[0]) for _ in range(w.layers)]
+    for l in range(w.layers):
+        stream.fill_cache(K[l], V[l], l, w.max_cache)
+    kept = torch.empty(w.layers, w.batch, w.kv_heads, w.budget, dtype=torch.int32, device=dev)
+    cfg = bkv.make_config(heads=w.heads, kv_heads=w.kv_heads, d=w.d, budget=w.budget,
+                          period=w.period, prefix=w.prefix, recent=w.recent, fps_cap=w.fps_cap,
+                          fps_keep=w.fps_keep, layers=w.layers, batch=w.batch,
+                          max_cache=w.max_cache, rope_theta=w.theta)
+    ws = torch.empty(bkv.bkv_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    cs = torch.cuda.current_stream(dev)
+    h = bkv.bkv_create(cfg, ws, cs)
+    import ctypes
+    kptr = (ctypes.c_void_p * w.layers)(*[t.data_ptr() for t in K])
+    vptr = (ctypes.c_void_p * w.layers)(*[t.data_ptr() for t in V])
+
+    # fill the query state: one append per decode step until the cache is full
+    for t in range(w.max_cache):
+        bkv.bkv_append_queries(h, stream.queries(), t)
+    qper = torch.stack([stream.queries() for _ in range(w.period)])  # reused every period
+    bkv.bkv_sync(h)
+    state = {"t": w.max_cache - 1}
+
+    def step():
+        t = state["t"]
+        bkv.bkv_evict_ptrs(h, kptr, vptr, w.max_cache, t, kept.data_ptr())
+        for i in range(w.period):
+            bkv.bkv_append_queries(h, qper[i], t + 1 + i)
+        state["t"] = t + w.period
+
+    for _ in range(args.warmup):
+        step()
+    bkv.bkv_sync(h)
+    st0 = bkv.bkv_get_stats(h)
+    heads_total = w.layers * w.batch * w.heads
+    R = w.group * (st0.beacons + min(w.period, w.fps_cap - w.fps_keep))
+    n_fps = st0.beacons + min(w.period, w.fps_cap - w.fps_keep)
+
+    sampler = ClockSampler(local_rank)
+    bkv.bkv_profile(h, True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cs)
+    for _ in range(args.steps):
+        step()
+    e1.record(cs)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    ktimes = bkv.bkv_profile_read(h)
+    bkv.bkv_profile(h, False)
+    bkv.bkv_sync(h)
+    st1 = bkv.bkv_get_stats(h)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    evictions_per_step = w.evictions_per_round
+    value = aggregate(evictions_per_step * args.steps, elapsed_ms / 1e3, world)
+
+    # ---- per-kernel roofline from the events recorded during the timed steps
+    peak, peak_kind = load_peaks()
+    rows_moved = (st1.rows_moved - st0.rows_moved) / args.steps
+    kb = kernel_bytes(w, R, rows_moved, heads_total, n_fps)
+    kernels = {}
+    for name, (ms, n) in ktimes.items():
+        if n == 0:
+            continue
+        per = ms / n
+        gbs = kb[name] / (per / 1e3) / 1e9 if kb[name] else None
+        kernels[name] = {"ms_per_launch": per, "launches_per_step": n / args.steps,
+                         "share": ms / sum(v[0] for v in ktimes.values()),
+                         "alg_bytes_per_launch": kb[name],
+                         "gbs": gbs, "frac": (gbs / peak) if gbs else None}
+    dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches_per_step"])
+    traffic = read_traffic(dom, w.name)
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak,
+                "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": traffic,
+                "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s"}
+    pbytes = path_bytes(w, R, rows_moved, heads_total)
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, bkv, h, K, V, kept, kptr, vptr, qper, state, dev, cs)
+        if world > 1:
+            tt = torch.tensor([e2e["elapsed_ms"]], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e["elapsed_ms"] = float(tt.item())
+        e2e = {"value": aggregate(evictions_per_step * e2e["steps"], e2e["elapsed_ms"] / 1e3, world),
+               "unit": "evictions/s", "h2d_bytes_per_step": e2e["h2d"],
+               "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"]}
+
+    bkv.bkv_destroy(h)
+    del K, V
+    torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        pool, cores = oracle_pool()
+        with pool:
+            r = oracle_rate(w, args.cpu_units, pool, cores)
+        cpu = {"value": r["value"], "unit": "evictions/s", "cores": r["cores"], "kind": "oracle",
+               "sample": f"{r['units']} steady-state units of {w.name} (one eviction = "
+                         f"{w.kv_heads} units), fp64 oracle, one unit per process, "
+                         f"{r['cpu_s']:.1f} s of CPU work in {r['wall_s']:.1f} s"}
+
+    if rank == 0:
+        out = {
+            "metric": "KV evictions/s (all layers x batch)", "value": value, "unit": "evictions/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "us_per_eviction": 1e3 * elapsed_ms / args.steps / evictions_per_step,
+            "config": {"workload": w.name, "layers": w.layers, "batch": w.batch,
+                       "heads": w.heads, "kv_heads": w.kv_heads, "d": w.d, "budget": w.budget,
+                       "period": w.period, "prefix": w.prefix, "recent": w.recent,
+                       "fps": f"{w.fps_cap}->{w.fps_keep}", "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (K/V cache %.1f GB)" % (
+                           2 * w.layers * w.batch * w.kv_heads * w.max_cache * w.d * 2 / 1e9),
+                       "step": f"1 eviction + {w.period} query appends"},
+            "gpu_launches": int(sum(n for _, n in ktimes.values())),
+            "roofline": roofline,
+            "path": {"alg_bytes_per_step": pbytes,
+                     "gbs": pbytes / (elapsed_ms / args.steps / 1e3) / 1e9,
+                     "frac": pbytes / (elapsed_ms / args.steps / 1e3) / 1e9 / peak,
+                     "rows_moved_per_unit": rows_moved / w.units, "obs_rows_per_unit": R},
+            "kernels": kernels,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, w, bkv, h, K, V, kept, kptr, vptr, qper, state, dev, cs):
+    """Same step through the C ABI, with each step's inputs coming from pinned
+    host memory (the period's queries and the new K/V rows) and the keep sets
+    going back to the host, all inside the timed region."""
+    import torch
+    q_host = qper.cpu().pin_memory()
+    tail = torch.empty(w.layers, 2, w.batch, w.kv_heads, w.period, w.d, dtype=torch.bfloat16)
+    for l in range(w.layers):
+        tail[l, 0] = K[l][:, :, w.budget:w.max_cache].cpu()
+        tail[l, 1] = V[l][:, :, w.budget:w.max_cache].cpu()
+    tail = tail.pin_memory()
+    kept_host = torch.empty(kept.shape, dtype=kept.dtype).pin_memory()
+    qdev = torch.empty_like(qper)
+
+    def step():
+        t = state["t"]
+        bkv.bkv_evict_ptrs(h, kptr, vptr, w.max_cache, t, kept.data_ptr())
+        kept_host.copy_(kept, non_blocking=True)
+        qdev.copy_(q_host, non_blocking=True)
+        for l in range(w.layers):
+            K[l][:, :, w.budget:w.max_cache].copy_(tail[l, 0], non_blocking=True)
+            V[l][:, :, w.budget:w.max_cache].copy_(tail[l, 1], non_blocking=True)
+        for i in range(w.period):
+            bkv.bkv_append_queries(h, qdev[i], t + 1 + i)
+        state["t"] = t + w.period
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cs)
+    for _ in range(args.steps):
+        step()
+    e1.record(cs)
+    torch.cuda.synchronize(dev)
+    bkv.bkv_sync(h)
+    return {"elapsed_ms": e0.elapsed_time(e1), "steps": args.steps,
+            "h2d": q_host.numel() * 2 + tail.numel() * 2, "d2h": kept_host.numel() * 4}
+
+
+def read_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the
+    current kernel source (profiles/traffic.md lists the source hash)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    src = {"compact": "k_compact.cu", "score_select": "k_score.cu", "fps": "k_fps.cu",
+           "append": "k_append.cu", "rope": "k_append.cu"}.get(kernel)
+    if not src or not os.path.exists(path):
+        return None
+    with open(os.path.join(ROOT, "kv_cache_eviction_head_gb300", "csrc", src), "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            cells = [c.strip() for c in line.strip().strip("|").split("|")]
+            if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload and cells[2] == digest:
+                try:
+                    return float(cells[3])
+                except ValueError:
+                    return None
+    return None
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3_4b_b192")
+    ap.add_argument("--cpu-units", type=int, default=192)
+    ap.add_argument("--ref-units-per-step", type=int, default=32)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    from synth import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

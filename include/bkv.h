@@ -1,0 +1,194 @@
+/*
+ * bkv.h - C ABI of the BeaconKV periodic KV-cache eviction step on one GPU.
+ *
+ * Method source: the page "BeaconKV：用历史查询代表保护长推理的远程回看" (reading
+ * notes on "BeaconKV: Key-Value Cache Compression Guided by Beacon Queries for
+ * Efficient Large Reasoning Model Inference"), cited as "BeaconKV reading
+ * notes" with its section and equation; buffer sizes 32 -> 16 and the 16+16
+ * split also appear in the rcap.io summary of the same paper.
+ *
+ * For every (sequence, layer, KV head) - a "unit" - an eviction
+ *   1. rotates each query head's beacon queries to the current step t and its
+ *      recent queries to their own positions (notes §2.3, Q_obs equation);
+ *   2. scores every cached key by softmax attention from those rows, max-pooled
+ *      over rows and over the query heads of the GQA group (§2.1 eqs. 4-5,
+ *      §2.3 eq. 7);
+ *   3. keeps the prefix, the recent window and the top-k scores up to the
+ *      budget, in slot order (§2.3 eq. 8);
+ *   4. compacts K and V in place to slots [0, budget);
+ *   5. compresses each query head's beacons + recents to fps_keep beacons by
+ *      farthest-point sampling (§2.2 Algorithm 1, eq. 9, Algorithm 2).
+ *
+ * Conventions shared by every call
+ *   - bf16 tensors are IEEE bfloat16, little-endian, contiguous, 16-byte
+ *     aligned device memory.
+ *   - Every call that launches work enqueues it on the handle's stream and
+ *     returns without waiting. Argument and state errors are found on the
+ *     host before anything is enqueued; they return a code and change nothing.
+ *   - Errors found on the device (non-finite inputs) are latched in a status
+ *     word in the workspace; bkv_sync returns and clears it.
+ *   - Nothing aborts, traps or throws across this boundary.
+ *   - The caller owns every pointer it passes (workspace, q_pre, K, V, kept).
+ *     They must stay valid until the enqueued work completes. The library
+ *     allocates no device memory; on the host it allocates the handle and,
+ *     while profiling is on, a pool of CUDA events.
+ *   - A handle is used from one host thread at a time.
+ */
+#ifndef BKV_H
+#define BKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct bkv_ctx* bkv_handle;
+
+typedef enum bkv_status {
+  BKV_OK = 0,
+  BKV_ERR_INVALID_ARG = 1, /* null or misaligned pointer, size out of range */
+  BKV_ERR_STATE = 2,       /* step out of order, cache_len not the tracked length */
+  BKV_ERR_WORKSPACE = 3,   /* workspace smaller than bkv_workspace_bytes() or misaligned */
+  BKV_ERR_CUDA = 4,        /* a CUDA runtime call failed */
+  BKV_ERR_NONFINITE = 5,   /* a query or key held Inf/NaN (latched on the device) */
+  BKV_ERR_TIMEOUT = 6,     /* a bounded device-side wait ran out (latched on the device) */
+  BKV_ERR_UNSUPPORTED = 7, /* shape the kernels do not implement (d != 128, too many rows) */
+  BKV_ERR_INTERNAL = 8     /* an internal consistency check failed */
+} bkv_status;
+
+/* Keep each eviction's Score[j] in the workspace for bkv_get_scores. */
+#define BKV_FLAG_KEEP_SCORES 1
+
+typedef struct bkv_config {
+  int32_t heads;      /* query heads per layer, H                                   */
+  int32_t kv_heads;   /* KV heads per layer, Hkv; H % Hkv == 0, G = H / Hkv         */
+  int32_t d;          /* head dimension; only 128 is implemented                    */
+  int32_t budget;     /* B_KV^min: slots each eviction keeps (notes §2.3 eq. 8)     */
+  int32_t period;     /* slots appended between evictions; the caller evicts at
+                         cache_len = budget + period (notes §2.1, Figure 5)         */
+  int32_t prefix;     /* n_prefix: leading slots always kept                        */
+  int32_t recent;     /* trailing slots always kept (the recent KV window)          */
+  int32_t fps_cap;    /* B_Q^max of eq. 9; 1 <= fps_cap <= 32                       */
+  int32_t fps_keep;   /* B_Q^min = n_beacon of eq. 9; 0 <= fps_keep < fps_cap.
+                         The recent-query ring holds n_rq = fps_cap - fps_keep.    */
+  int32_t layers;     /* 1..128                                                     */
+  int32_t batch;      /* sequences                                                  */
+  int32_t max_cache;  /* slot capacity of each K/V tensor; > budget                 */
+  double rope_theta;  /* RoPE base; inv_freq_i = theta^(-2i/d), rotate-half pairs   */
+  int32_t flags;      /* BKV_FLAG_* bits                                            */
+} bkv_config;
+
+typedef struct bkv_stats {
+  uint64_t evictions;      /* bkv_evict calls completed on the host side              */
+  uint64_t fps_calls;      /* FPS launches (each covers every query head)             */
+  uint64_t rows_moved;     /* K/V rows copied by compaction, summed over units (device) */
+  int32_t beacons;         /* current beacons per query head                          */
+  int32_t recents;         /* current recent queries per query head                   */
+  int32_t cache_len;       /* cache length the library expects at the next evict      */
+  int64_t last_step;       /* step of the last bkv_append_queries, -1 before the first */
+} bkv_stats;
+
+/* Bytes of device workspace a handle with this config needs (>= 256-B aligned
+ * base required). Holds per query head the beacon buffer (fps_cap x d bf16),
+ * the recent ring (n_rq x d bf16) and the last FPS trace, a RoPE table, the
+ * status word and, with BKV_FLAG_KEEP_SCORES, layers*batch*kv_heads*max_cache
+ * fp32 scores. Errors: BKV_ERR_INVALID_ARG for a null pointer or an invalid
+ * config, BKV_ERR_UNSUPPORTED for d != 128 or fps_cap > 32. */
+bkv_status bkv_workspace_bytes(const bkv_config* cfg, size_t* bytes);
+
+/* Creates a handle over a caller-allocated workspace (device pointer) and a
+ * CUDA stream (cudaStream_t, may be NULL for the legacy default stream).
+ * Enqueues the zeroing of the library state. The stream starts with an empty
+ * cache and no query state. */
+bkv_status bkv_create(const bkv_config* cfg, void* workspace, size_t workspace_bytes,
+                      void* cuda_stream, bkv_handle* out);
+
+/* Makes later calls enqueue on another stream. The caller orders the two
+ * streams (the library records no event). */
+bkv_status bkv_set_stream(bkv_handle h, void* cuda_stream);
+
+/* One decode step: pushes each query head's pre-RoPE query of step `step`
+ * into its recent ring; when the ring already holds n_rq queries its oldest
+ * moves to the end of the beacon buffer, and when that buffer reaches fps_cap
+ * it is compressed to fps_keep rows by farthest-point sampling (notes §2.2,
+ * eq. 9). The caller appends the step's key and value to cache slot
+ * cache_len itself; the library counts that slot.
+ *   q_pre: device bf16 [layers][batch][heads][d].
+ *   step:  absolute position of this token; the first call may use any
+ *          step >= 0, every later one must be the previous step + 1
+ *          (BKV_ERR_STATE otherwise). The counted cache length may not exceed
+ *          max_cache (BKV_ERR_STATE: evict first). */
+bkv_status bkv_append_queries(bkv_handle h, const void* q_pre, int64_t step);
+
+/* The eviction step at time t = step (notes §2.3 eqs. 7-8, Algorithm 2).
+ *   K, V:  host arrays of `layers` device pointers; each points to a bf16
+ *          [batch][kv_heads][max_cache][d] cache whose slots [0, cache_len)
+ *          hold post-RoPE keys / values in position order.
+ *   cache_len: must equal the length the library counted (budget after the
+ *          previous eviction plus one per append since), with
+ *          budget < cache_len <= max_cache; BKV_ERR_STATE otherwise.
+ *   step:  must equal the step of the last bkv_append_queries.
+ *   kept:  device int32 [layers][batch][kv_heads][budget]; receives I_final,
+ *          ascending slot indices into the pre-eviction cache.
+ * On completion slots [0, budget) of every unit hold K[I_final] / V[I_final];
+ * slots [budget, cache_len) are left with unspecified contents. Then every
+ * query head's beacons become FPS(beacons + recents, fps_keep) and its recent
+ * ring is emptied. BKV_ERR_UNSUPPORTED if G * (beacons + recents) > 256. */
+bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache_len,
+                     int64_t step, int32_t* kept);
+
+/* Waits for the handle's stream, then returns and clears the latched device
+ * status (BKV_OK when no device error was seen), or BKV_ERR_CUDA. */
+bkv_status bkv_sync(bkv_handle h);
+
+/* Copies the pick order of the last FPS call of every query head into host
+ * memory: int8 [layers][batch][heads][fps_keep], indices into that call's
+ * candidate list (beacons oldest first, then recents oldest first), -1 where
+ * fewer than fps_keep candidates existed. Synchronizes the stream.
+ * n: bytes available at host_out. */
+bkv_status bkv_get_fps_trace(bkv_handle h, int8_t* host_out, size_t n);
+
+/* Copies the last eviction's Score[j] into host memory: fp32
+ * [layers][batch][kv_heads][max_cache], entries j >= cache_len unspecified.
+ * Needs BKV_FLAG_KEEP_SCORES (BKV_ERR_STATE otherwise). Synchronizes.
+ * n: floats available at host_out. */
+bkv_status bkv_get_scores(bkv_handle h, float* host_out, size_t n);
+
+/* Copies one query head's current beacons (rows [0, beacons)) and recent
+ * ring (slot s holds the query of the step tau with tau % n_rq == s) into
+ * host memory: bf16 [fps_cap + n_rq][d]. Synchronizes. Debug and tests. */
+bkv_status bkv_get_head_state(bkv_handle h, int32_t layer, int32_t seq, int32_t head,
+                              uint16_t* host_out, size_t n);
+
+/* Per-kernel device time, from CUDA events the library records on its stream
+ * around each of its launches while profiling is on. Index with BKV_K_*. */
+enum { BKV_K_APPEND = 0, BKV_K_ROPE = 1, BKV_K_SCORE = 2, BKV_K_COMPACT = 3, BKV_K_FPS = 4,
+       BKV_K_COUNT = 5 };
+typedef struct bkv_kernel_times {
+  double ms[BKV_K_COUNT];          /* summed launch durations, milliseconds */
+  uint64_t launches[BKV_K_COUNT];  /* launches summed */
+} bkv_kernel_times;
+
+/* enable != 0: start recording (and zero the sums); 0: stop recording.
+ * Events come from a host-side pool the handle owns; no device memory. */
+bkv_status bkv_profile(bkv_handle h, int32_t enable);
+
+/* Synchronizes the stream and returns the sums since profiling was enabled. */
+bkv_status bkv_profile_read(bkv_handle h, bkv_kernel_times* out);
+
+/* Counters and bookkeeping; synchronizes to read the device counter. */
+bkv_status bkv_get_stats(bkv_handle h, bkv_stats* out);
+
+/* Frees the handle (not the workspace). Enqueued work must be complete. */
+void bkv_destroy(bkv_handle h);
+
+/* Static string naming a status code. */
+const char* bkv_status_str(bkv_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BKV_H */

@@ -1,0 +1,211 @@
+"""Thin ctypes binding of libbkv (include/bkv.h), same names as the C ABI.
+
+Argument marshalling only: tensors become device pointers, a torch stream
+becomes its cudaStream_t, status codes become exceptions. Every step of the
+eviction runs in the library's CUDA kernels. The library must be built
+(`kv_cache_eviction_head_gb300.build.build()`); importing this module without
+it raises ImportError.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libbkv.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is missing: build it with kv_cache_eviction_head_gb300.build.build()")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+BKV_OK = 0
+BKV_ERR_INVALID_ARG = 1
+BKV_ERR_STATE = 2
+BKV_ERR_WORKSPACE = 3
+BKV_ERR_CUDA = 4
+BKV_ERR_NONFINITE = 5
+BKV_ERR_TIMEOUT = 6
+BKV_ERR_UNSUPPORTED = 7
+BKV_ERR_INTERNAL = 8
+BKV_FLAG_KEEP_SCORES = 1
+
+EXPORTED = ["bkv_workspace_bytes", "bkv_create", "bkv_set_stream", "bkv_append_queries",
+            "bkv_evict", "bkv_sync", "bkv_get_fps_trace", "bkv_get_scores", "bkv_get_head_state",
+            "bkv_profile", "bkv_profile_read", "bkv_get_stats", "bkv_destroy", "bkv_status_str"]
+KERNELS = ["append", "rope", "score_select", "compact", "fps"]
+
+
+class BkvConfig(ctypes.Structure):
+    _fields_ = [("heads", ctypes.c_int32), ("kv_heads", ctypes.c_int32), ("d", ctypes.c_int32),
+                ("budget", ctypes.c_int32), ("period", ctypes.c_int32), ("prefix", ctypes.c_int32),
+                ("recent", ctypes.c_int32), ("fps_cap", ctypes.c_int32), ("fps_keep", ctypes.c_int32),
+                ("layers", ctypes.c_int32), ("batch", ctypes.c_int32), ("max_cache", ctypes.c_int32),
+                ("rope_theta", ctypes.c_double), ("flags", ctypes.c_int32)]
+
+
+class BkvStats(ctypes.Structure):
+    _fields_ = [("evictions", ctypes.c_uint64), ("fps_calls", ctypes.c_uint64),
+                ("rows_moved", ctypes.c_uint64), ("beacons", ctypes.c_int32),
+                ("recents", ctypes.c_int32), ("cache_len", ctypes.c_int32),
+                ("last_step", ctypes.c_int64)]
+
+
+class BkvKernelTimes(ctypes.Structure):
+    _fields_ = [("ms", ctypes.c_double * 5), ("launches", ctypes.c_uint64 * 5)]
+
+
+_vp, _sz, _i32, _i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64
+_lib.bkv_workspace_bytes.argtypes = [ctypes.POINTER(BkvConfig), ctypes.POINTER(_sz)]
+_lib.bkv_create.argtypes = [ctypes.POINTER(BkvConfig), _vp, _sz, _vp, ctypes.POINTER(_vp)]
+_lib.bkv_set_stream.argtypes = [_vp, _vp]
+_lib.bkv_append_queries.argtypes = [_vp, _vp, _i64]
+_lib.bkv_evict.argtypes = [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _i64, _vp]
+_lib.bkv_sync.argtypes = [_vp]
+_lib.bkv_get_fps_trace.argtypes = [_vp, _vp, _sz]
+_lib.bkv_get_scores.argtypes = [_vp, _vp, _sz]
+_lib.bkv_get_head_state.argtypes = [_vp, _i32, _i32, _i32, _vp, _sz]
+_lib.bkv_get_stats.argtypes = [_vp, ctypes.POINTER(BkvStats)]
+_lib.bkv_profile.argtypes = [_vp, _i32]
+_lib.bkv_profile_read.argtypes = [_vp, ctypes.POINTER(BkvKernelTimes)]
+_lib.bkv_destroy.argtypes = [_vp]
+_lib.bkv_destroy.restype = None
+_lib.bkv_status_str.argtypes = [_i32]
+_lib.bkv_status_str.restype = ctypes.c_char_p
+for _n in EXPORTED[:-2]:
+    getattr(_lib, _n).restype = ctypes.c_int
+
+
+class BkvError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {bkv_status_str(code)}")
+
+
+def bkv_status_str(code: int) -> str:
+    return _lib.bkv_status_str(int(code)).decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != BKV_OK:
+        raise BkvError(code, where)
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        return 0
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def make_config(*, heads, kv_heads, d, budget, period, prefix, recent, fps_cap=32, fps_keep=16,
+                layers, batch, max_cache, rope_theta, flags=0) -> BkvConfig:
+    return BkvConfig(heads, kv_heads, d, budget, period, prefix, recent, fps_cap, fps_keep, layers,
+                     batch, max_cache, float(rope_theta), flags)
+
+
+def bkv_workspace_bytes(cfg: BkvConfig) -> int:
+    n = _sz(0)
+    _check(_lib.bkv_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n)), "bkv_workspace_bytes")
+    return n.value
+
+
+@dataclass
+class Handle:
+    ptr: int
+    cfg: BkvConfig
+    workspace: object  # keeps the caller's workspace tensor alive
+
+
+def bkv_create(cfg: BkvConfig, workspace, stream=None) -> Handle:
+    """workspace: a uint8 CUDA tensor of at least bkv_workspace_bytes(cfg) bytes."""
+    out = _vp(0)
+    _check(_lib.bkv_create(ctypes.byref(cfg), _vp(workspace.data_ptr()), _sz(workspace.numel() * workspace.element_size()),
+                           _vp(_stream_ptr(stream)), ctypes.byref(out)), "bkv_create")
+    return Handle(out.value, cfg, workspace)
+
+
+def bkv_set_stream(h: Handle, stream) -> None:
+    _check(_lib.bkv_set_stream(_vp(h.ptr), _vp(_stream_ptr(stream))), "bkv_set_stream")
+
+
+def bkv_append_queries(h: Handle, q_pre, step: int) -> None:
+    """q_pre: bf16 CUDA tensor [layers][batch][heads][d], contiguous."""
+    _check(_lib.bkv_append_queries(_vp(h.ptr), _vp(q_pre.data_ptr()), _i64(step)), "bkv_append_queries")
+
+
+def bkv_evict(h: Handle, K, V, cache_len: int, step: int, kept) -> None:
+    """K, V: sequences of `layers` bf16 CUDA tensors [batch][kv_heads][max_cache][d];
+    kept: int32 CUDA tensor [layers][batch][kv_heads][budget]."""
+    n = len(K)
+    kp = (_vp * n)(*[t.data_ptr() for t in K])
+    vp = (_vp * n)(*[t.data_ptr() for t in V])
+    _check(_lib.bkv_evict(_vp(h.ptr), kp, vp, _i32(cache_len), _i64(step), _vp(kept.data_ptr())),
+           "bkv_evict")
+
+
+def bkv_evict_ptrs(h: Handle, kptrs, vptrs, cache_len: int, step: int, kept_ptr: int) -> None:
+    """bkv_evict with raw device pointers (pre-marshalled pointer arrays allowed)."""
+    _check(_lib.bkv_evict(_vp(h.ptr), kptrs, vptrs, _i32(cache_len), _i64(step), _vp(kept_ptr)),
+           "bkv_evict")
+
+
+def bkv_sync(h: Handle) -> None:
+    _check(_lib.bkv_sync(_vp(h.ptr)), "bkv_sync")
+
+
+def bkv_get_fps_trace(h: Handle) -> np.ndarray:
+    c = h.cfg
+    out = np.empty((c.layers, c.batch, c.heads, c.fps_keep), dtype=np.int8)
+    _check(_lib.bkv_get_fps_trace(_vp(h.ptr), _vp(out.ctypes.data), _sz(out.nbytes)), "bkv_get_fps_trace")
+    return out
+
+
+def bkv_get_scores(h: Handle) -> np.ndarray:
+    c = h.cfg
+    out = np.empty((c.layers, c.batch, c.kv_heads, c.max_cache), dtype=np.float32)
+    _check(_lib.bkv_get_scores(_vp(h.ptr), _vp(out.ctypes.data), _sz(out.size)), "bkv_get_scores")
+    return out
+
+
+def bkv_get_head_state(h: Handle, layer: int, seq: int, head: int) -> np.ndarray:
+    """uint16 [fps_cap + n_rq][d]: beacon rows, then the recent ring slots."""
+    c = h.cfg
+    out = np.empty((c.fps_cap + c.fps_cap - c.fps_keep, c.d), dtype=np.uint16)
+    _check(_lib.bkv_get_head_state(_vp(h.ptr), layer, seq, head, _vp(out.ctypes.data), _sz(out.size)),
+           "bkv_get_head_state")
+    return out
+
+
+def bkv_profile(h: Handle, enable: bool) -> None:
+    _check(_lib.bkv_profile(_vp(h.ptr), _i32(1 if enable else 0)), "bkv_profile")
+
+
+def bkv_profile_read(h: Handle) -> dict:
+    """{kernel name: (summed ms, launches)} since profiling was enabled."""
+    t = BkvKernelTimes()
+    _check(_lib.bkv_profile_read(_vp(h.ptr), ctypes.byref(t)), "bkv_profile_read")
+    return {k: (t.ms[i], int(t.launches[i])) for i, k in enumerate(KERNELS)}
+
+
+def bkv_get_stats(h: Handle) -> BkvStats:
+    s = BkvStats()
+    _check(_lib.bkv_get_stats(_vp(h.ptr), ctypes.byref(s)), "bkv_get_stats")
+    return s
+
+
+def bkv_destroy(h: Handle) -> None:
+    if h.ptr:
+        _lib.bkv_destroy(_vp(h.ptr))
+        h.ptr = 0
+
+
+def raw_status(fn_name: str, *args) -> int:
+    """Calls a C entry point and returns its status code (tests of the error paths)."""
+    return getattr(_lib, fn_name)(*args)
+
+
+def library_path() -> str:
+    return _LIB_PATH

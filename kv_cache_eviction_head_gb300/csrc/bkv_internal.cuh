@@ -1,0 +1,91 @@
+// Internal declarations shared by the host API and the kernels of libbkv.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bkv.h"
+
+namespace bkv {
+
+constexpr int kD = 128;             // head dimension the kernels implement
+constexpr int kMaxLayers = 128;     // per-layer K/V pointers travel in the launch parameters
+constexpr int kMaxObsRows = 256;    // observation rows per unit (G * (beacons + recents))
+constexpr int kMaxFpsCap = 32;      // one warp lane per FPS candidate
+constexpr int kRopePairs = kD / 2;
+
+// Device-side error latch: the first error code wins.
+__device__ __forceinline__ void latch(uint32_t* status, uint32_t code) {
+  if (status) atomicCAS(status, 0u, code);
+}
+
+// ---------------------------------------------------------------------------
+// append: push one query per query head into its recent ring
+struct AppendParams {
+  const uint4* q;           // [heads_total][d] bf16 as 16 uint4 per row
+  uint4* bq;                // [heads_total][fps_cap][d]
+  uint4* rq;                // [heads_total][n_rq][d]
+  int64_t heads_total;
+  int fps_cap, n_rq;
+  int slot;                 // ring slot of this step (step % n_rq)
+  int spill;                // 1: the ring is full; its oldest row moves to bq[nb] first
+  int nb;                   // beacons before this push
+};
+cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
+
+// RoPE cos/sin table: row 0 is the eviction step t, row 1 + k the k-th oldest recent
+struct RopeParams {
+  float2* tab;              // [rows][kRopePairs] (cos, sin)
+  int64_t t;
+  int nr;                   // recent rows; rows = 1 + nr
+  double theta;
+};
+cudaError_t launch_rope_table(const RopeParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// farthest-point sampling of every query head's candidate set
+struct FpsParams {
+  uint4* bq;                // [heads_total][fps_cap][d]; rows [0, nb) are candidates, output too
+  const uint4* rq;          // [heads_total][n_rq][d]; nr recents follow the beacons
+  int8_t* trace;            // [heads_total][m]
+  uint32_t* status;
+  int64_t heads_total;
+  int fps_cap, n_rq;
+  int nb, nr;               // candidates: nb beacons then nr recents (N = nb + nr <= 32)
+  int ring_first;           // ring slot of the oldest recent
+  int m;                    // rows kept (fps_keep)
+};
+cudaError_t launch_fps(const FpsParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// score + keep-set selection, one CTA per unit
+struct ScoreParams {
+  const uint4* bq;          // [layers][batch][heads][fps_cap][d]
+  const uint4* rq;          // [layers][batch][heads][n_rq][d]
+  const float2* rope;       // [1 + nr][kRopePairs]
+  const __nv_bfloat16* K[kMaxLayers];
+  int32_t* kept;            // [units][budget]
+  float* scores;            // [units][max_cache] or null
+  uint32_t* status;
+  int batch, kv_heads, group, fps_cap, n_rq;
+  int nb, nr, ring_first;
+  int L, budget, prefix, recent, max_cache;
+  int units;
+};
+cudaError_t launch_score_select(const ScoreParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// in-place gather of the kept rows, one CTA per unit
+struct CompactParams {
+  __nv_bfloat16* K[kMaxLayers];
+  __nv_bfloat16* V[kMaxLayers];
+  const int32_t* kept;      // [units][budget]
+  unsigned long long* rows_moved;
+  uint32_t* status;
+  int batch, kv_heads, budget, max_cache, units;
+  int L;                    // pre-eviction cache length; every kept slot is < L
+};
+cudaError_t launch_compact(const CompactParams& p, cudaStream_t s);
+
+}  // namespace bkv

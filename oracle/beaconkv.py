@@ -282,13 +282,17 @@ class UnitOracle:
         W = attention_weights(Q, qpos, bf16_to_f64(np.stack(self.K)), np.asarray(self.pos))
         return max_pool(W), Q.shape[0]
 
-    def evict(self, t: int, kept_override=None) -> EvictResult:
+    def evict(self, t: int, kept_override=None, score=None) -> EvictResult:
         """One eviction at time t. `kept_override`, when given, is a keep set the
         caller has already checked against this oracle's own one (a different
         but equally valid choice inside the score tie band); compaction and the
-        following state then use it."""
+        following state then use it. `score`, when given, is this unit's
+        scores(t) computed just before (saves recomputing it)."""
         L = len(self.K)
-        score, nobs = self.scores(t)
+        if score is None:
+            score, nobs = self.scores(t)
+        else:
+            nobs = self.observation(t)[0].shape[0]
         kept = select_keep(score, L, self.prefix, self.recent, self.budget)
         use = list(kept_override) if kept_override is not None else kept
         self.K = [self.K[i] for i in use]

@@ -1,0 +1,157 @@
+"""GPU parity of the CUDA library against the CPU oracle, through the C ABI.
+
+Each case runs a seeded synthetic stream through both sides in lockstep
+(tests/lockstep.py states the agreement rules) and at sizes the oracle
+finishes in seconds: several 128-key tiles plus a ragged tail, every
+observation-row count the configs reach, zero beacons, short and long
+periods, GQA groups 1..8, and inputs that drive FPS through its wide-exponent
+exact-sum path.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from synth import WORKLOADS
+from tests.lockstep import run_lockstep
+
+pytestmark = pytest.mark.gpu
+
+TINY = WORKLOADS["tiny"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from kv_cache_eviction_head_gb300.build import build
+    build()
+
+
+def assert_clean(rep, min_evictions=1):
+    assert not rep.failures, "\n".join(rep.failures)
+    assert rep.evictions >= min_evictions
+    assert rep.units_checked >= rep.evictions
+
+
+def test_tiny_full_stream():
+    rep = run_lockstep(TINY, seed=0xBEAC0)
+    assert_clean(rep, min_evictions=24)
+    assert rep.fps_heads_checked == 4 * rep.evictions
+
+
+@pytest.mark.parametrize("name,over", [
+    ("zero_beacons", dict(fps_cap=16, fps_keep=0)),
+    ("short_period", dict(period=8)),
+    ("long_period", dict(period=24)),
+    ("no_prefix_no_recent", dict(prefix=0, recent=0)),
+    ("gqa1", dict(heads=1, kv_heads=1)),
+    ("gqa7", dict(heads=7, kv_heads=1)),
+    ("gqa8_two_kv", dict(heads=16, kv_heads=2)),
+    ("ragged_budget", dict(budget=200, steps=300)),
+    ("small_buffer", dict(fps_cap=6, fps_keep=2)),
+    ("batch_layers", dict(layers=2, batch=3, heads=8, kv_heads=2, steps=200)),
+])
+def test_tiny_variants(name, over):
+    w = TINY.with_(**{"steps": 240, **over})
+    rep = run_lockstep(w, seed=0xBEAC0 + len(name))
+    assert_clean(rep)
+
+
+def test_many_tiles():
+    w = TINY.with_(budget=1000, steps=1100, heads=8, kv_heads=2)
+    rep = run_lockstep(w, seed=7)
+    assert_clean(rep, min_evictions=6)
+
+
+def test_qwen3_4b_b1_first_eviction_sampled_units():
+    w = WORKLOADS["qwen3_4b_b1"]
+    units = [(0, 0, 0), (5, 0, 3), (17, 0, 7), (35, 0, 1), (20, 0, 4), (35, 0, 7)]
+    rep = run_lockstep(w, seed=0xBEAC1, sample_units=units, steps=w.budget + w.period + 32)
+    assert_clean(rep)
+    assert rep.units_checked == len(units)
+
+
+def wide_queries(t, q):
+    """Replaces some queries by vectors whose exponents span far more than 20
+    binades (FPS's wide exact-sum path), by zero rows and by exact duplicates."""
+    g = torch.Generator().manual_seed(t)
+    out = q.clone()
+    if t % 3 == 0:
+        e = torch.randint(-60, 8, (q.shape[-1],), generator=g).float()
+        s = torch.where(torch.rand(q.shape[-1], generator=g) < 0.5, -1.0, 1.0)
+        out[..., 0, :] = (s * (1 + torch.rand(q.shape[-1], generator=g)) * torch.exp2(e)).to(q.dtype)
+    if t % 7 == 0:
+        out[..., 1, :] = 0
+    if t % 5 == 0:
+        out[..., 2, :] = out[..., 3, :]
+    return out
+
+
+def test_fps_wide_exponents_zero_rows_duplicates():
+    w = TINY.with_(steps=300)
+    rep = run_lockstep(w, seed=3, query_hook=wide_queries)
+    assert_clean(rep)
+
+
+def test_step_order_and_cache_length_are_validated():
+    from kv_cache_eviction_head_gb300 import bkv
+    w = TINY
+    dev = torch.device("cuda")
+    cfg = bkv.make_config(heads=4, kv_heads=1, d=128, budget=w.budget, period=16, prefix=4,
+                          recent=16, layers=1, batch=1, max_cache=w.max_cache, rope_theta=1e6)
+    ws = torch.empty(bkv.bkv_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    h = bkv.bkv_create(cfg, ws, torch.cuda.current_stream())
+    q = torch.randn(1, 1, 4, 128, device=dev).to(torch.bfloat16)
+    K = [torch.zeros(1, 1, w.max_cache, 128, dtype=torch.bfloat16, device=dev)]
+    kept = torch.empty(1, 1, 1, w.budget, dtype=torch.int32, device=dev)
+    try:
+        with pytest.raises(bkv.BkvError) as e:
+            bkv.bkv_evict(h, K, K, 5, 0, kept)           # nothing appended yet
+        assert e.value.code == bkv.BKV_ERR_STATE
+        bkv.bkv_append_queries(h, q, 10)
+        with pytest.raises(bkv.BkvError) as e:
+            bkv.bkv_append_queries(h, q, 12)             # skipped a step
+        assert e.value.code == bkv.BKV_ERR_STATE
+        with pytest.raises(bkv.BkvError) as e:
+            bkv.bkv_append_queries(h, torch.empty(513, dtype=torch.bfloat16, device=dev)[1:], 11)
+        assert e.value.code == bkv.BKV_ERR_INVALID_ARG   # misaligned pointer
+        for t in range(11, 11 + w.budget + 15):
+            bkv.bkv_append_queries(h, q, t)
+        last = 10 + w.budget + 15
+        with pytest.raises(bkv.BkvError) as e:
+            bkv.bkv_evict(h, K, K, w.budget + 15, last, kept)  # not the counted length
+        assert e.value.code == bkv.BKV_ERR_STATE
+        with pytest.raises(bkv.BkvError) as e:
+            bkv.bkv_evict(h, K, K, w.budget + 16, last - 1, kept)  # not the last step
+        assert e.value.code == bkv.BKV_ERR_STATE
+        with pytest.raises(bkv.BkvError) as e:
+            bkv.bkv_append_queries(h, q, last + 1)         # cache would exceed max_cache
+        assert e.value.code == bkv.BKV_ERR_STATE
+        bkv.bkv_evict(h, K, K, w.budget + 16, last, kept)
+        bkv.bkv_sync(h)
+        st = bkv.bkv_get_stats(h)
+        assert (st.cache_len, st.beacons, st.recents, st.evictions) == (w.budget, 16, 0, 1)
+    finally:
+        bkv.bkv_destroy(h)
+
+
+def test_nonfinite_query_is_latched_not_trapped():
+    from kv_cache_eviction_head_gb300 import bkv
+    dev = torch.device("cuda")
+    cfg = bkv.make_config(heads=4, kv_heads=1, d=128, budget=64, period=16, prefix=4, recent=16,
+                          fps_cap=4, fps_keep=2, layers=1, batch=1, max_cache=80, rope_theta=1e6)
+    ws = torch.empty(bkv.bkv_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    h = bkv.bkv_create(cfg, ws, torch.cuda.current_stream())
+    try:
+        for t in range(6):
+            q = torch.randn(1, 1, 4, 128, device=dev).to(torch.bfloat16)
+            if t == 1:
+                q[0, 0, 2, 5] = float("nan")
+            bkv.bkv_append_queries(h, q, t)    # the 6th push runs FPS over the NaN row
+        with pytest.raises(bkv.BkvError) as e:
+            bkv.bkv_sync(h)
+        assert e.value.code == bkv.BKV_ERR_NONFINITE
+        bkv.bkv_sync(h)                         # the latch was cleared
+    finally:
+        bkv.bkv_destroy(h)
