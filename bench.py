@@ -252,16 +252,25 @@ def run_ours(args, w):
     # fill the query state: one append per decode step until the cache is full
     for t in range(w.max_cache):
         bkv.bkv_append_queries(h, stream.queries(), t)
-    qper = torch.stack([stream.queries() for _ in range(w.period)])  # reused every period
+    # every period gets the stream's next queries (a repeated period would hand
+    # FPS exact duplicates, which no decode stream produces)
+    n_periods = args.warmup + args.steps          # device-resident runs use [0, n_periods)
+    qpool = torch.empty(2 * n_periods, w.period, w.layers, w.batch, w.heads, w.d, dtype=torch.bfloat16,
+                        device=dev)
+    for p in range(2 * n_periods):             # the e2e run uses the second half
+        for i in range(w.period):
+            qpool[p, i] = stream.queries()
     bkv.bkv_sync(h)
-    state = {"t": w.max_cache - 1}
+    state = {"t": w.max_cache - 1, "p": 0}
 
     def step():
         t = state["t"]
+        qper = qpool[state["p"] % n_periods]
         bkv.bkv_evict_ptrs(h, kptr, vptr, w.max_cache, t, kept.data_ptr())
         for i in range(w.period):
             bkv.bkv_append_queries(h, qper[i], t + 1 + i)
         state["t"] = t + w.period
+        state["p"] += 1
 
     for _ in range(args.warmup):
         step()
@@ -321,7 +330,7 @@ def run_ours(args, w):
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, bkv, h, K, V, kept, kptr, vptr, qper, state, dev, cs)
+        e2e = run_e2e(args, w, bkv, h, K, V, kept, kptr, vptr, qpool[n_periods:], state, dev, cs)
         if world > 1:
             tt = torch.tensor([e2e["elapsed_ms"]], device=dev)
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -376,32 +385,35 @@ def run_ours(args, w):
     return 0
 
 
-def run_e2e(args, w, bkv, h, K, V, kept, kptr, vptr, qper, state, dev, cs):
+def run_e2e(args, w, bkv, h, K, V, kept, kptr, vptr, qpool, state, dev, cs):
     """Same step through the C ABI, with each step's inputs coming from pinned
     host memory (the period's queries and the new K/V rows) and the keep sets
     going back to the host, all inside the timed region."""
     import torch
-    q_host = qper.cpu().pin_memory()
+    q_host = qpool.cpu().pin_memory()  # one period of queries per step, host side
     tail = torch.empty(w.layers, 2, w.batch, w.kv_heads, w.period, w.d, dtype=torch.bfloat16)
     for l in range(w.layers):
         tail[l, 0] = K[l][:, :, w.budget:w.max_cache].cpu()
         tail[l, 1] = V[l][:, :, w.budget:w.max_cache].cpu()
     tail = tail.pin_memory()
     kept_host = torch.empty(kept.shape, dtype=kept.dtype).pin_memory()
-    qdev = torch.empty_like(qper)
+    qdev = torch.empty_like(qpool[0])
+    n_periods = qpool.shape[0]
 
     def step():
         t = state["t"]
         bkv.bkv_evict_ptrs(h, kptr, vptr, w.max_cache, t, kept.data_ptr())
         kept_host.copy_(kept, non_blocking=True)
-        qdev.copy_(q_host, non_blocking=True)
+        qdev.copy_(q_host[state["e"] % n_periods], non_blocking=True)
         for l in range(w.layers):
             K[l][:, :, w.budget:w.max_cache].copy_(tail[l, 0], non_blocking=True)
             V[l][:, :, w.budget:w.max_cache].copy_(tail[l, 1], non_blocking=True)
         for i in range(w.period):
             bkv.bkv_append_queries(h, qdev[i], t + 1 + i)
         state["t"] = t + w.period
+        state["e"] += 1
 
+    state["e"] = 0
     for _ in range(max(1, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
@@ -413,7 +425,7 @@ def run_e2e(args, w, bkv, h, K, V, kept, kptr, vptr, qper, state, dev, cs):
     torch.cuda.synchronize(dev)
     bkv.bkv_sync(h)
     return {"elapsed_ms": e0.elapsed_time(e1), "steps": args.steps,
-            "h2d": q_host.numel() * 2 + tail.numel() * 2, "d2h": kept_host.numel() * 4}
+            "h2d": qdev.numel() * 2 + tail.numel() * 2, "d2h": kept_host.numel() * 4}
 
 
 def read_traffic(kernel: str, workload: str):

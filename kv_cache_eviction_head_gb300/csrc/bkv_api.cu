@@ -7,10 +7,6 @@
 
 #include "bkv_internal.cuh"
 
-namespace bkv {
-size_t score_smem_bytes(int R, int L);
-}
-
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -264,7 +260,7 @@ bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache
   sp.bq = h->bq();
   sp.rq = h->rq();
   sp.rope = h->rope();
-  for (int l = 0; l < c.layers; ++l) sp.K[l] = static_cast<const __nv_bfloat16*>(K[l]);
+  if (!bkv::encode_kmaps(sp, K, c.layers, c.batch, c.kv_heads, c.max_cache)) return BKV_ERR_CUDA;
   sp.kept = kept;
   sp.scores = h->scores();
   sp.status = h->status();

@@ -1,7 +1,9 @@
 // Internal declarations shared by the host API and the kernels of libbkv.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -59,12 +61,12 @@ struct FpsParams {
 cudaError_t launch_fps(const FpsParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
-// score + keep-set selection, one CTA per unit
+// score + keep-set selection: persistent CTAs over the units
 struct ScoreParams {
+  CUtensorMap kmap[kMaxLayers];  // per layer: K as 2-D [batch*kv_heads*max_cache][d] bf16
   const uint4* bq;          // [layers][batch][heads][fps_cap][d]
   const uint4* rq;          // [layers][batch][heads][n_rq][d]
   const float2* rope;       // [1 + nr][kRopePairs]
-  const __nv_bfloat16* K[kMaxLayers];
   int32_t* kept;            // [units][budget]
   float* scores;            // [units][max_cache] or null
   uint32_t* status;
@@ -74,6 +76,11 @@ struct ScoreParams {
   int units;
 };
 cudaError_t launch_score_select(const ScoreParams& p, cudaStream_t s);
+// Dynamic shared memory the score kernel needs (huge when the shape does not fit).
+size_t score_smem_bytes(int R, int L);
+// Fills p.kmap for K[0..layers) (host; no device allocation). False on failure.
+bool encode_kmaps(ScoreParams& p, const void* const* K, int layers, int batch, int kv_heads,
+                  int max_cache);
 
 // ---------------------------------------------------------------------------
 // in-place gather of the kept rows, one CTA per unit
