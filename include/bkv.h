@@ -178,6 +178,39 @@ bkv_status bkv_profile(bkv_handle h, int32_t enable);
 /* Synchronizes the stream and returns the sums since profiling was enabled. */
 bkv_status bkv_profile_read(bkv_handle h, bkv_kernel_times* out);
 
+/* Score + keep-set selection of one eviction without a handle or workspace.
+ * The BeaconKV paper has no counterpart: this is a deployment variant of the
+ * scoring step of bkv_evict for callers that cannot allocate device memory -
+ * code running from a fixed, pre-sized memory arena, runtimes that forbid
+ * cudaMalloc after start-up because it can synchronize the device, plugins
+ * that may only use the buffers their host passes in. It allocates nothing:
+ * its one scratch buffer, the RoPE cos/sin table of the eviction step
+ * (16,896 bytes), is a file-scope __device__ array that every GPU loading the
+ * library holds until the process exits.
+ *   cfg:      as bkv_create (flags ignored).
+ *   bq:       device bf16 [layers][batch][heads][fps_cap][d]; rows [0, beacons)
+ *             of each query head are its pre-RoPE beacons, oldest first.
+ *   rq:       device bf16 [layers][batch][heads][fps_cap - fps_keep][d]; the
+ *             recent queries of steps step - recents + 1 .. step, the query of
+ *             step tau in slot tau % (fps_cap - fps_keep).
+ *   beacons:  0 <= beacons < fps_cap; recents: 0 <= recents <= fps_cap - fps_keep
+ *             and at most 32 (BKV_ERR_UNSUPPORTED beyond: the scratch holds
+ *             1 + 32 table rows).
+ *   K, cache_len, step, kept: as bkv_evict, but cache_len is only checked
+ *             against budget < cache_len <= max_cache. Nothing else is written:
+ *             no compaction, no FPS, no state.
+ *   cuda_stream: where the work is enqueued.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Every call rewrites the whole table before using
+ * it; calls whose work overlaps on the GPU share the array and race, so order
+ * them. Device-side conditions (non-finite scores) are not reported here;
+ * host checks return BKV_ERR_INVALID_ARG / BKV_ERR_UNSUPPORTED / BKV_ERR_CUDA. */
+bkv_status bkv_score_select_noalloc(const bkv_config* cfg, const void* bq, const void* rq,
+                                    int32_t beacons, int32_t recents, void* const* K,
+                                    int32_t cache_len, int64_t step, int32_t* kept,
+                                    void* cuda_stream);
+
 /* Counters and bookkeeping; synchronizes to read the device counter. */
 bkv_status bkv_get_stats(bkv_handle h, bkv_stats* out);
 

@@ -33,7 +33,8 @@ BKV_FLAG_KEEP_SCORES = 1
 
 EXPORTED = ["bkv_workspace_bytes", "bkv_create", "bkv_set_stream", "bkv_append_queries",
             "bkv_evict", "bkv_sync", "bkv_get_fps_trace", "bkv_get_scores", "bkv_get_head_state",
-            "bkv_profile", "bkv_profile_read", "bkv_get_stats", "bkv_destroy", "bkv_status_str"]
+            "bkv_profile", "bkv_profile_read", "bkv_score_select_noalloc", "bkv_get_stats",
+            "bkv_destroy", "bkv_status_str"]
 KERNELS = ["append", "rope", "score_select", "compact", "fps"]
 
 
@@ -69,6 +70,8 @@ _lib.bkv_get_head_state.argtypes = [_vp, _i32, _i32, _i32, _vp, _sz]
 _lib.bkv_get_stats.argtypes = [_vp, ctypes.POINTER(BkvStats)]
 _lib.bkv_profile.argtypes = [_vp, _i32]
 _lib.bkv_profile_read.argtypes = [_vp, ctypes.POINTER(BkvKernelTimes)]
+_lib.bkv_score_select_noalloc.argtypes = [ctypes.POINTER(BkvConfig), _vp, _vp, _i32, _i32,
+                                          ctypes.POINTER(_vp), _i32, _i64, _vp, _vp]
 _lib.bkv_destroy.argtypes = [_vp]
 _lib.bkv_destroy.restype = None
 _lib.bkv_status_str.argtypes = [_i32]
@@ -188,6 +191,19 @@ def bkv_profile_read(h: Handle) -> dict:
     t = BkvKernelTimes()
     _check(_lib.bkv_profile_read(_vp(h.ptr), ctypes.byref(t)), "bkv_profile_read")
     return {k: (t.ms[i], int(t.launches[i])) for i, k in enumerate(KERNELS)}
+
+
+def bkv_score_select_noalloc(cfg: BkvConfig, bq, rq, beacons: int, recents: int, K,
+                             cache_len: int, step: int, kept, stream=None) -> None:
+    """Score + keep-set selection without a handle or workspace (see include/bkv.h).
+    bq, rq: bf16 CUDA tensors in the state layout; K: `layers` bf16 CUDA tensors;
+    kept: int32 CUDA tensor [layers][batch][kv_heads][budget]."""
+    n = len(K)
+    kp = (_vp * n)(*[t.data_ptr() for t in K])
+    _check(_lib.bkv_score_select_noalloc(ctypes.byref(cfg), _vp(bq.data_ptr()), _vp(rq.data_ptr()),
+                                         _i32(beacons), _i32(recents), kp, _i32(cache_len),
+                                         _i64(step), _vp(kept.data_ptr()), _vp(_stream_ptr(stream))),
+           "bkv_score_select_noalloc")
 
 
 def bkv_get_stats(h: Handle) -> BkvStats:
