@@ -2,8 +2,9 @@
 """Throughput of the BeaconKV eviction step on GB300, one JSON line on stdout.
 
 A step is one eviction period of the whole hot path for every layer and
-sequence of the workload: one bkv_evict (RoPE table, fused score + keep-set
-selection, in-place K/V compaction, FPS of beacons + recents) followed by the
+sequence of the workload: one bkv_evict (RoPE table, one fused kernel for
+scoring, keep-set selection and in-place K/V compaction, FPS of beacons +
+recents) followed by the
 period's bkv_append_queries calls (one per decode step). The metric is
 evictions per second, one eviction being one (layer, sequence) pair.
 
@@ -114,8 +115,9 @@ def kernel_bytes(w, R: int, rows_moved_per_launch: float, heads_total: int, n_fp
     units = w.units
     row = w.d * 2
     return {
-        "score_select": units * (L * row + R * row + w.budget * 4),
-        "compact": 4 * row * rows_moved_per_launch + units * w.budget * 4,
+        # scoring reads K once and the rows, writes the keep set; the fused
+        # compaction reads the moved V rows and writes the moved K and V rows
+        "score_select": units * (L * row + R * row + w.budget * 4) + 3 * row * rows_moved_per_launch,
         "fps": heads_total * (n_fps * row + w.fps_keep * (row + 1)),
         "append": heads_total * 2 * row,
         "rope": 0,
@@ -433,7 +435,7 @@ def read_traffic(kernel: str, workload: str):
     current kernel source (profiles/traffic.md lists the source hash)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.md")
-    src = {"compact": "k_compact.cu", "score_select": "k_score.cu", "fps": "k_fps.cu",
+    src = {"score_select": "k_score.cu", "fps": "k_fps.cu",
            "append": "k_append.cu", "rope": "k_append.cu"}.get(kernel)
     if not src or not os.path.exists(path):
         return None
@@ -457,6 +459,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_4b_b192")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--cpu-units", type=int, default=192)
     ap.add_argument("--ref-units-per-step", type=int, default=32)
     ap.add_argument("--no-e2e", action="store_true")
@@ -466,6 +470,8 @@ def main():
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     from synth import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(batch=args.batch, name=f"{w.name}_batch{args.batch}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -164,8 +164,8 @@ bkv_status bkv_get_head_state(bkv_handle h, int32_t layer, int32_t seq, int32_t 
 
 /* Per-kernel device time, from CUDA events the library records on its stream
  * around each of its launches while profiling is on. Index with BKV_K_*. */
-enum { BKV_K_APPEND = 0, BKV_K_ROPE = 1, BKV_K_SCORE = 2, BKV_K_COMPACT = 3, BKV_K_FPS = 4,
-       BKV_K_COUNT = 5 };
+enum { BKV_K_APPEND = 0, BKV_K_ROPE = 1, BKV_K_SCORE = 2 /* score, keep set and compaction */,
+       BKV_K_FPS = 3, BKV_K_COUNT = 4 };
 typedef struct bkv_kernel_times {
   double ms[BKV_K_COUNT];          /* summed launch durations, milliseconds */
   uint64_t launches[BKV_K_COUNT];  /* launches summed */

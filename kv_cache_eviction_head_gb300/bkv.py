@@ -35,7 +35,7 @@ EXPORTED = ["bkv_workspace_bytes", "bkv_create", "bkv_set_stream", "bkv_append_q
             "bkv_evict", "bkv_sync", "bkv_get_fps_trace", "bkv_get_scores", "bkv_get_head_state",
             "bkv_profile", "bkv_profile_read", "bkv_score_select_noalloc", "bkv_get_stats",
             "bkv_destroy", "bkv_status_str"]
-KERNELS = ["append", "rope", "score_select", "compact", "fps"]
+KERNELS = ["append", "rope", "score_select", "fps"]
 
 
 class BkvConfig(ctypes.Structure):
@@ -54,7 +54,7 @@ class BkvStats(ctypes.Structure):
 
 
 class BkvKernelTimes(ctypes.Structure):
-    _fields_ = [("ms", ctypes.c_double * 5), ("launches", ctypes.c_uint64 * 5)]
+    _fields_ = [("ms", ctypes.c_double * 4), ("launches", ctypes.c_uint64 * 4)]
 
 
 _vp, _sz, _i32, _i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64

@@ -110,15 +110,19 @@ struct bkv_ctx {
   }
   // Runs `launch` between two recorded events when profiling is on.
   template <class F>
-  cudaError_t timed(int kernel, F launch) {
+  cudaError_t timed(int kernel, cudaStream_t on, F launch) {
     if (!prof) return launch();
     cudaEvent_t a = take_event(), b = take_event();
     if (!a || !b) return cudaErrorMemoryAllocation;
-    cudaEventRecord(a, stream);
+    cudaEventRecord(a, on);
     const cudaError_t e = launch();
-    cudaEventRecord(b, stream);
+    cudaEventRecord(b, on);
     marks.push_back({kernel, a, b});
     return e;
+  }
+  template <class F>
+  cudaError_t timed(int kernel, F launch) {
+    return timed(kernel, stream, launch);
   }
   ~bkv_ctx() {
     for (auto& m : marks) {
@@ -140,7 +144,7 @@ struct bkv_ctx {
   int ring_slot(int64_t step) const { return (int)(((step % n_rq) + n_rq) % n_rq); }
 };
 
-static bkv_status launch_fps_all(bkv_handle h, int nb, int nr, int ring_first) {
+static bkv_status launch_fps_all(bkv_handle h, int nb, int nr, int ring_first, cudaStream_t on) {
   bkv::FpsParams f{};
   f.bq = h->bq();
   f.rq = h->rq();
@@ -153,7 +157,7 @@ static bkv_status launch_fps_all(bkv_handle h, int nb, int nr, int ring_first) {
   f.nr = nr;
   f.ring_first = ring_first;
   f.m = h->cfg.fps_keep;
-  if (h->timed(BKV_K_FPS, [&] { return bkv::launch_fps(f, h->stream); }) != cudaSuccess)
+  if (h->timed(BKV_K_FPS, on, [&] { return bkv::launch_fps(f, on); }) != cudaSuccess)
     return BKV_ERR_CUDA;
   h->fps_calls++;
   return BKV_OK;
@@ -227,7 +231,7 @@ bkv_status bkv_append_queries(bkv_handle h, const void* q_pre, int64_t step) {
   h->last_step = step;
   h->cache_len++;
   if (h->nb >= h->cfg.fps_cap) {  // eq. 9: compress a full beacon buffer
-    const bkv_status st = launch_fps_all(h, h->nb, 0, 0);
+    const bkv_status st = launch_fps_all(h, h->nb, 0, 0, h->stream);
     if (st != BKV_OK) return st;
     h->nb = h->cfg.fps_keep;
   }
@@ -245,7 +249,7 @@ bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache
     return BKV_ERR_STATE;
   const int R = h->group * (h->nb + h->nr);
   if (R > bkv::kMaxObsRows || cache_len > 8192) return BKV_ERR_UNSUPPORTED;
-  if (bkv::score_smem_bytes(R, cache_len) > kMaxSmem) return BKV_ERR_UNSUPPORTED;
+  if (bkv::score_smem_bytes(R, cache_len, h->nr, c.budget, 1) > kMaxSmem) return BKV_ERR_UNSUPPORTED;
 
   const int ring_first = h->ring_slot(step - h->nr + 1);
   bkv::RopeParams rp{};
@@ -278,29 +282,20 @@ bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache
   sp.recent = c.recent;
   sp.max_cache = c.max_cache;
   sp.units = (int)h->units;
+  for (int l = 0; l < c.layers; ++l) {
+    sp.Kc[l] = static_cast<__nv_bfloat16*>(K[l]);
+    sp.Vc[l] = static_cast<__nv_bfloat16*>(V[l]);
+  }
+  sp.rows_moved = h->rows_moved();
+  sp.compact = 1;
   if (h->timed(BKV_K_SCORE, [&] { return bkv::launch_score_select(sp, h->stream); }) != cudaSuccess)
     return BKV_ERR_CUDA;
 
-  bkv::CompactParams cp{};
-  for (int l = 0; l < c.layers; ++l) {
-    cp.K[l] = static_cast<__nv_bfloat16*>(K[l]);
-    cp.V[l] = static_cast<__nv_bfloat16*>(V[l]);
-  }
-  cp.kept = kept;
-  cp.rows_moved = h->rows_moved();
-  cp.status = h->status();
-  cp.L = cache_len;
-  cp.batch = c.batch;
-  cp.kv_heads = c.kv_heads;
-  cp.budget = c.budget;
-  cp.max_cache = c.max_cache;
-  cp.units = (int)h->units;
-  if (h->timed(BKV_K_COMPACT, [&] { return bkv::launch_compact(cp, h->stream); }) != cudaSuccess)
-    return BKV_ERR_CUDA;
-
   // Algorithm 2: the next period starts from FPS(beacons + recents)
-  const bkv_status st = launch_fps_all(h, h->nb, h->nr, ring_first);
-  if (st != BKV_OK) return st;
+  {
+    const bkv_status st = launch_fps_all(h, h->nb, h->nr, ring_first, h->stream);
+    if (st != BKV_OK) return st;
+  }
   const int n = h->nb + h->nr;
   h->nb = n > c.fps_keep ? c.fps_keep : n;
   h->nr = 0;

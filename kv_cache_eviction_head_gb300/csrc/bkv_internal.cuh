@@ -74,25 +74,17 @@ struct ScoreParams {
   int nb, nr, ring_first;
   int L, budget, prefix, recent, max_cache;
   int units;
+  // in-place compaction of the kept rows (null pointers / compact = 0: none)
+  __nv_bfloat16* Kc[kMaxLayers];
+  __nv_bfloat16* Vc[kMaxLayers];
+  unsigned long long* rows_moved;
+  int compact;
 };
 cudaError_t launch_score_select(const ScoreParams& p, cudaStream_t s);
 // Dynamic shared memory the score kernel needs (huge when the shape does not fit).
-size_t score_smem_bytes(int R, int L);
+size_t score_smem_bytes(int R, int L, int nr, int budget, int compact);
 // Fills p.kmap for K[0..layers) (host; no device allocation). False on failure.
 bool encode_kmaps(ScoreParams& p, const void* const* K, int layers, int batch, int kv_heads,
                   int max_cache);
-
-// ---------------------------------------------------------------------------
-// in-place gather of the kept rows, one CTA per unit
-struct CompactParams {
-  __nv_bfloat16* K[kMaxLayers];
-  __nv_bfloat16* V[kMaxLayers];
-  const int32_t* kept;      // [units][budget]
-  unsigned long long* rows_moved;
-  uint32_t* status;
-  int batch, kv_heads, budget, max_cache, units;
-  int L;                    // pre-eviction cache length; every kept slot is < L
-};
-cudaError_t launch_compact(const CompactParams& p, cudaStream_t s);
 
 }  // namespace bkv

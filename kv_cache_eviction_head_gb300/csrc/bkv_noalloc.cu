@@ -80,7 +80,7 @@ extern "C" bkv_status bkv_score_select_noalloc(const bkv_config* c, const void* 
   const int group = c->heads / c->kv_heads;
   const int R = group * (beacons + recents);
   if (units > 0x7FFFFFFF || R > bkv::kMaxObsRows || cache_len > 8192 ||
-      bkv::score_smem_bytes(R, cache_len) > 227 * 1024)
+      bkv::score_smem_bytes(R, cache_len, recents, c->budget, 0) > 227 * 1024)
     return BKV_ERR_UNSUPPORTED;
 
   float2* scratch = nullptr;
@@ -116,6 +116,7 @@ extern "C" bkv_status bkv_score_select_noalloc(const bkv_config* c, const void* 
   sp.recent = c->recent;
   sp.max_cache = c->max_cache;
   sp.units = (int)units;
+  sp.compact = 0;  // score and keep set only
   if (bkv::launch_score_select(sp, s) != cudaSuccess) return BKV_ERR_CUDA;
   return BKV_OK;
 }

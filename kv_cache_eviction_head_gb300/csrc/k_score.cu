@@ -30,11 +30,12 @@
 //              pass 2  D[key][row] = K_tile . Q^T   (M = 128 keys, N = rows)
 //            so each epilogue thread owns one TMEM lane (a row in pass 1, a
 //            key in pass 2) and reduces along its own registers only;
-//   warp 2   builds the next unit's rotated rows while the tensor cores finish
-//            the current unit;
+//   warp 2   warms L2 with the next unit's source rows;
 //   warp 3   selects the keep set of a finished unit from its scores;
-//   warps 4-7  epilogue: TMEM -> registers, online log-sum-exp in pass 1,
-//            max-pooling in pass 2, scores to shared memory.
+//   warps 4-11  epilogue, two warpgroups taking alternate TMEM buffers:
+//            TMEM -> registers, online log-sum-exp in pass 1, max-pooling in
+//            pass 2, scores to shared memory; between units they build the
+//            next unit's rotated rows (the tensor cores wait for them).
 // Every cross-warp wait is a bounded wait on an mbarrier; on expiry the kernel
 // latches BKV_ERR_TIMEOUT, every role stops at its next wait, outstanding
 // copies are drained and the TMEM is freed before the CTA exits.
@@ -50,11 +51,11 @@ namespace bkv {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kTileKeys = 128;
 constexpr int kSlabBytes = kTileKeys * 128;   // 128 rows x 64 bf16: one SWIZZLE_128B box
 constexpr int kTileBytes = 2 * kSlabBytes;    // 32 KB per 128-key tile
-constexpr int kEpiThreads = 128;              // warps 4-7
+constexpr int kEpiThreads = 128;              // one epilogue warpgroup (warps 4-7 or 8-11)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s: far beyond any legitimate wait
 constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -115,6 +116,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+
+// Non-tensor bulk copies: global -> shared with an mbarrier, shared -> global
+// in bulk groups.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
@@ -184,132 +203,166 @@ __device__ __forceinline__ float fast_log2(float x) {
   return y;
 }
 
-__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(kFull, v, off);
-    if (lane >= off) v += o;
-  }
-  return v;
+// Keep set of one unit from its scores sc[0, L), written ascending to out. One
+// warp. The D = L - budget dropped slots are the D smallest keys
+// (score bits, ~slot) among the candidates [prefix, L - recent): lower score
+// first, and among equal scores the higher slot first, so the lower slot wins
+// a tie. Each lane keeps the kList smallest keys of its own candidates; the
+// warp extracts the global minimum D times, and a lane whose list runs dry
+// rescans for the keys above the last one it gave up. dropped[] is a bitmask
+// over slots in shared memory.
+constexpr int kList = 8;
+__device__ __forceinline__ bool key_less(uint32_t ah, uint32_t al, uint32_t bh, uint32_t bl) {
+  return ah < bh || (ah == bh && al < bl);
 }
-
-// Keep set of one unit from its scores sc[0, L), written ascending to out.
-// One warp. Returns false if the kept count came out wrong (never expected).
-__device__ bool select_keep(const float* sc, int L, int prefix, int recent, int budget, int32_t* out,
-                            unsigned* hist) {
+__device__ void select_keep(const float* sc, int L, int prefix, int recent, int budget, int32_t* out,
+                            uint32_t* dropped, int* drops) {
   const int lane = threadIdx.x & 31;
   const int c0 = prefix < L ? prefix : L;
   const int c1 = L - recent > c0 ? L - recent : c0;
-  uint32_t want = 0, mask = 0;
-  int k = L - budget;  // rank (1-based) of the threshold among the candidates
-  int n_eq = 0;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int b = lane; b < 256; b += 32) hist[b] = 0;
-    __syncwarp();
-    for (int j = c0 + lane; j < c1; j += 32) {
-      const uint32_t key = __float_as_uint(sc[j]);
-      if ((key & mask) == want) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-    }
-    __syncwarp();
-    int cnt = 0;
+  const int D = L - budget;
+  const uint32_t none = 0xFFFFFFFFu;
+  for (int wd = lane; wd < (L + 31) / 32; wd += 32) dropped[wd] = 0u;
+  // lane-local sorted lists of (hi = score bits, lo = ~slot)
+  uint32_t lh[kList], ll[kList];
+  auto fill = [&](uint32_t after_h, uint32_t after_l) {
 #pragma unroll
-    for (int b = 0; b < 8; ++b) cnt += (int)hist[lane * 8 + b];
-    const int incl = warp_incl_scan(cnt, lane);
-    const int excl = incl - cnt;
-    const unsigned hit = __ballot_sync(kFull, excl < k && k <= incl);
-    const int src = hit ? __ffs(hit) - 1 : 0;
-    int digit = 0, kk = k, hb_sel = 0;
-    if (lane == src) {
-      int cum = excl;
-      for (int b = 0; b < 8; ++b) {
-        const int hb = (int)hist[lane * 8 + b];
-        if (cum + hb >= k) {
-          digit = lane * 8 + b;
-          kk = k - cum;
-          hb_sel = hb;
-          break;
+    for (int i = 0; i < kList; ++i) {
+      lh[i] = none;
+      ll[i] = none;
+    }
+    for (int j = c0 + lane; j < c1; j += 32) {
+      const uint32_t kh = __float_as_uint(sc[j]), kl = ~(uint32_t)j;
+      if (!key_less(after_h, after_l, kh, kl)) continue;  // already given up
+      if (!key_less(kh, kl, lh[kList - 1], ll[kList - 1])) continue;
+      uint32_t ch = kh, cl = kl;
+#pragma unroll
+      for (int i = 0; i < kList; ++i) {  // insertion into the sorted list
+        if (key_less(ch, cl, lh[i], ll[i])) {
+          const uint32_t th = lh[i], tl = ll[i];
+          lh[i] = ch;
+          ll[i] = cl;
+          ch = th;
+          cl = tl;
         }
-        cum += hb;
       }
     }
-    digit = __shfl_sync(kFull, digit, src);
-    k = __shfl_sync(kFull, kk, src);
-    n_eq = __shfl_sync(kFull, hb_sel, src);
-    want |= (uint32_t)digit << shift;
-    mask |= 0xFFu << shift;
-    __syncwarp();
-  }
-  const uint32_t T = want;
-  const int keep_eq = n_eq - k;  // the lowest-slot keep_eq candidates equal to T stay
-  // lanes take contiguous slot ranges so the scans preserve slot order
-  const int chunk = (L + 31) / 32;
-  const int j0 = min(lane * chunk, L), j1 = min(j0 + chunk, L);
-  int my_eq = 0;
-  for (int j = j0; j < j1; ++j)
-    if (j >= c0 && j < c1 && __float_as_uint(sc[j]) == T) ++my_eq;
-  int eq_rank = warp_incl_scan(my_eq, lane) - my_eq;
-  const int eq_start = eq_rank;
-  int my_keep = 0;
-  for (int j = j0; j < j1; ++j) {
-    bool keep = true;
-    if (j >= c0 && j < c1) {
-      const uint32_t key = __float_as_uint(sc[j]);
-      if (key < T) keep = false;
-      else if (key == T) keep = eq_rank++ < keep_eq;
+  };
+  fill(0u, 0u);
+  // (0, 0) precedes every real key except score 0 at slot 0xFFFFFFFF, which cannot occur
+  uint32_t last_h = 0u, last_l = 0u;
+  int used = 0;
+  __syncwarp();
+  for (int d = 0; d < D; ++d) {
+    uint32_t mh = lh[0], ml = ll[0];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const uint32_t oh = __shfl_xor_sync(kFull, mh, off), ol = __shfl_xor_sync(kFull, ml, off);
+      if (key_less(oh, ol, mh, ml)) {
+        mh = oh;
+        ml = ol;
+      }
     }
-    my_keep += keep;
-  }
-  const int incl = warp_incl_scan(my_keep, lane);
-  const int total = __shfl_sync(kFull, incl, 31);
-  if (total != budget) return false;
-  int dst = incl - my_keep;
-  eq_rank = eq_start;
-  for (int j = j0; j < j1; ++j) {
-    bool keep = true;
-    if (j >= c0 && j < c1) {
-      const uint32_t key = __float_as_uint(sc[j]);
-      if (key < T) keep = false;
-      else if (key == T) keep = eq_rank++ < keep_eq;
+    const int slot = (int)(~ml);
+    if (lane == 0) atomicOr(&dropped[slot >> 5], 1u << (slot & 31));
+    if (lh[0] == mh && ll[0] == ml) {  // this lane owned it: pop, refill when empty
+      last_h = mh;
+      last_l = ml;
+#pragma unroll
+      for (int i = 0; i < kList - 1; ++i) {
+        lh[i] = lh[i + 1];
+        ll[i] = ll[i + 1];
+      }
+      lh[kList - 1] = none;
+      ll[kList - 1] = none;
+      if (++used == kList) {
+        fill(last_h, last_l);
+        used = 0;
+      }
     }
-    if (keep) out[dst++] = j;
   }
-  return true;
+  __syncwarp();
+  // kept slots in ascending order, written 32 at a time; dropped slots likewise
+  int base = 0, dbase = 0;
+  for (int j0 = 0; j0 < L; j0 += 32) {
+    const int j = j0 + lane;
+    const bool drop = j < L && ((dropped[j >> 5] >> (j & 31)) & 1u);
+    const bool keep = j < L && !drop;
+    const unsigned lt = (1u << lane) - 1u;
+    const unsigned m = __ballot_sync(kFull, keep), dm = __ballot_sync(kFull, drop);
+    if (keep) out[base + __popc(m & lt)] = j;
+    if (drop && drops) drops[dbase + __popc(dm & lt)] = j;
+    base += __popc(m);
+    dbase += __popc(dm);
+  }
 }
 
+constexpr int kChunkRows = 32;                   // rows per compaction chunk
+constexpr int kChunkBytes = kChunkRows * kD * 2;  // 8 KB
+
 struct Layout {
-  int R, Rp16, mtiles, qrows;  // rows, rows rounded to 16, M tiles of 128 rows, rows allocated
-  int ntiles, Lp, stages, bufcols;
-  size_t q_hi, q_lo, kst, sc, lse, lim, bars, misc, total;
+  int R, Rp16, mtiles, qrows, rows64;  // rows, rows to 16, M tiles, rows allocated, rows to 64
+  int ntiles, Lp, stages, bufcols, cbufs, scbufs, D;
+  size_t q_hi, q_lo, kst, cst, sc, lse, lim, part, rowinfo, drops, bars, misc, total;
 };
 
-__host__ __device__ inline Layout make_layout(int R, int L) {
+// Shared-memory plan. The fixed part holds the observation rows (bf16 hi and
+// lo), the per-row statistics and tables; the rest goes to K-tile stages,
+// compaction chunks and score buffers, in the first arrangement that fits:
+// two or more K stages always, eight / four / two 8 KB compaction chunks when
+// compacting, two score buffers (one when nothing else fits).
+__host__ __device__ inline Layout make_layout(int R, int L, int nr, int budget, int compact) {
   Layout s;
   s.R = R;
   s.Rp16 = (R + 15) & ~15;
   s.mtiles = R > 128 ? 2 : 1;
   s.qrows = s.Rp16 > 128 ? s.Rp16 : 128;  // a second M tile covers rows [Rp16 - 128, Rp16)
+  s.rows64 = (s.Rp16 + 63) / 64 * 64 > s.qrows ? (s.Rp16 + 63) / 64 * 64 : s.qrows;  // pass-2 column chunks
   s.ntiles = (L + kTileKeys - 1) / kTileKeys;
   s.Lp = s.ntiles * kTileKeys;
   s.bufcols = (s.mtiles > 1 || s.Rp16 > 128) ? 256 : 128;
+  s.D = L - budget;
   const size_t qbytes = ((size_t)s.qrows * 256 + 1023) / 1024 * 1024;  // two 128-byte slabs per row
+  const size_t small = (size_t)s.rows64 * 8 + (size_t)s.qrows * 16 + (size_t)s.qrows * 8 +
+                       (compact ? 2 * (size_t)s.D * 4 + 16 : 0) + 64 * 8 + 2048 + 64;
+  const size_t cap = 227 * 1024 - 1024;  // 1 KB kept for aligning the dynamic base
+  const size_t scb = (size_t)s.Lp * 4;
+  static const int plans[][3] = {{4, 0, 2}, {3, 0, 2}, {2, 0, 2}, {2, 0, 1}};          // no compaction
+  static const int cplans[][3] = {{2, 8, 2}, {2, 4, 2}, {2, 2, 2}, {2, 2, 1}};         // compaction
+  s.stages = 0;
+  s.cbufs = 0;
+  s.scbufs = 0;
+  for (int i = 0; i < 4; ++i) {
+    const int* pl = compact ? cplans[i] : plans[i];
+    const size_t need = 2 * qbytes + (size_t)pl[0] * kTileBytes + (size_t)pl[1] * kChunkBytes + pl[2] * scb + small;
+    if (need <= cap) {
+      s.stages = pl[0];
+      s.cbufs = pl[1];
+      s.scbufs = pl[2];
+      break;
+    }
+  }
   size_t off = 0;
   s.q_hi = off;
   off += qbytes;
   s.q_lo = off;
   off += qbytes;
   s.kst = off;  // 1024-aligned
-  const size_t tail = 2 * (size_t)s.Lp * 4 + (size_t)s.qrows * 8 + 64 * 8 + 2048;
-  const size_t cap = 227 * 1024 - 1024;  // 1 KB kept for aligning the dynamic base
-  const long long room = (long long)cap - (long long)off - (long long)tail;
-  const int st = room > 0 ? (int)(room / kTileBytes) : 0;
-  s.stages = st > 4 ? 4 : st;
   off += (size_t)s.stages * kTileBytes;
+  s.cst = off;
+  off += (size_t)s.cbufs * kChunkBytes;
   s.sc = off;
-  off += 2 * (size_t)s.Lp * 4;
+  off += (size_t)s.scbufs * scb;
   s.lse = off;
-  off += (size_t)s.qrows * 4;
+  off += (size_t)s.rows64 * 4;
   s.lim = off;
-  off += (size_t)s.qrows * 4;
+  off += (size_t)s.rows64 * 4;
+  s.part = off;
+  off += (size_t)s.qrows * 16;
+  s.rowinfo = off;
+  off += (size_t)s.qrows * 8;
+  s.drops = off;
+  off += compact ? 2 * (size_t)s.D * 4 + 16 : 0;
   s.bars = (off + 7) & ~(size_t)7;
   off = s.bars + 64 * 8;
   s.misc = off;
@@ -332,13 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per_head = P.nb + P.nr;
-  const Layout lay = make_layout(P.group * per_head, P.L);
+  const Layout lay = make_layout(P.group * per_head, P.L, P.nr, P.budget, P.compact);
   const int R = lay.R, L = P.L, T = lay.ntiles, S = lay.stages;
 
   unsigned char* q_hi = smem + lay.q_hi;
   unsigned char* q_lo = smem + lay.q_lo;
   unsigned char* kst = smem + lay.kst;
-  float* sc = reinterpret_cast<float*>(smem + lay.sc);    // [2][Lp]
+  float* sc = reinterpret_cast<float*>(smem + lay.sc);    // [scbufs][Lp]
   float* lse = reinterpret_cast<float*>(smem + lay.lse);  // [qrows], log2 units
   int* lim = reinterpret_cast<int*>(smem + lay.lim);      // [qrows], exclusive key bound per row
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
@@ -350,9 +403,19 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   uint64_t* qfree = bars + 13;
   uint64_t* sready = bars + 14;  // [2]
   uint64_t* sfree = bars + 16;   // [2]
+  uint64_t* cfull = bars + 20;   // [8] compaction chunks landed in shared memory
+  uint64_t* dready = bars + 28;  // [2] a unit's drop list is ready
+  uint64_t* dfree = bars + 30;   // [2] the copier is done with a drop list
+  unsigned char* cst = smem + lay.cst;                       // [cbufs][8 KB] compaction chunks
+  int* dlist = reinterpret_cast<int*>(smem + lay.drops);     // [2][D] dropped slots, ascending
+  const int NSC = lay.scbufs;                                // score buffers (1 or 2)
   uint64_t* lsebar = bars + 18;
+  uint64_t* lse2bar = bars + 19;
+  float* pm = reinterpret_cast<float*>(smem + lay.part);  // [2][qrows] per-group running max
+  float* pz = pm + 2 * lay.qrows;                         // [2][qrows] per-group running sum
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + lay.misc);
-  unsigned* hist = reinterpret_cast<unsigned*>(smem + lay.misc + 64);  // [256]
+  uint32_t* dropbits = reinterpret_cast<uint32_t*>(smem + lay.misc + 64);  // [ceil(L/32)], <= 8192 slots
+  int2* rowinfo = reinterpret_cast<int2*>(smem + lay.rowinfo);             // [R] source offset, table row
 
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
@@ -361,26 +424,42 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], kEpiThreads);
-      mbar_init(&sready[i], kEpiThreads);
+      mbar_init(&tempty[i], kEpiThreads);       // one group consumes each buffer
+      mbar_init(&sready[i], 2 * kEpiThreads);
       mbar_init(&sfree[i], 32);
     }
-    mbar_init(qready, 32);
+    mbar_init(qready, 2 * kEpiThreads);  // the epilogue warps build the rows
     mbar_init(qfree, 1);
-    mbar_init(lsebar, kEpiThreads);
+    for (int i = 0; i < lay.cbufs; ++i) mbar_init(&cfull[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&dready[i], 32);
+      mbar_init(&dfree[i], 1);
+    }
+    mbar_init(lsebar, 2 * kEpiThreads);
+    mbar_init(lse2bar, 2 * kEpiThreads);
     ctl->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   // zero both row buffers once: padding rows stay zero for the whole launch
   for (int i = tid; i < (int)(2 * (lay.q_lo - lay.q_hi) / 16); i += kThreads)
     reinterpret_cast<uint4*>(q_hi)[i] = make_uint4(0, 0, 0, 0);
-  for (int r = tid; r < lay.qrows; r += kThreads) {
+  for (int r = tid; r < lay.rows64; r += kThreads) {
     int bound = 0;
     if (r < R) {
       const int w = r % per_head;
       bound = w < P.nb ? L : L - P.nr + (w - P.nb) + 1;
     }
     lim[r] = bound;
+  }
+  // per-launch table: each observation row's source
+  for (int r = tid; r < R; r += kThreads) {
+    const int gi = r / per_head, w = r % per_head;
+    if (w < P.nb) {
+      rowinfo[r] = make_int2((gi * P.fps_cap + w) * 16, 0);
+    } else {
+      const int kq = w - P.nb;
+      rowinfo[r] = make_int2(((gi * P.n_rq + (P.ring_first + kq) % P.n_rq) * 16) | (1 << 30), 1 + kq);
+    }
   }
   const uint32_t ncols = 2 * (uint32_t)lay.bufcols;
   if (warp == 1) tmem_alloc(&ctl->tmem_base, ncols);
@@ -390,6 +469,75 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   const int mine = P.units > (int)blockIdx.x ? (P.units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+
+  const float qk_scale = kLog2e * rsqrtf((float)kD);  // rows carry 1/sqrt(d) and log2(e)
+  const uint32_t slab_q = (uint32_t)lay.qrows * 128;
+  auto head_base = [&](int it) -> int64_t {
+    int layer, seq, kvh;
+    unit_geom(blockIdx.x + it * gridDim.x, P.batch, P.kv_heads, layer, seq, kvh);
+    return ((int64_t)layer * P.batch + seq) * (P.kv_heads * P.group) + (int64_t)kvh * P.group;
+  };
+  // source row of observation row r and its RoPE table row
+  auto row_src = [&](int64_t head0, int r, int& prow) -> const uint4* {
+    const int2 info = rowinfo[r];
+    prow = info.y;
+    const uint4* base = (info.x & (1 << 30)) ? P.rq + head0 * P.n_rq * 16 : P.bq + head0 * P.fps_cap * 16;
+    return base + (info.x & ~(1 << 30));
+  };
+  // Rotated observation rows of unit `it`, split into bf16 hi + lo, written in
+  // the SWIZZLE_128B K-major layout; thread t of n builds items t, t + n, ...
+  auto build_rows = [&](int it, int t, int n) {
+    constexpr int kBatch = 4;  // items per thread with loads in flight together
+    const int64_t head0 = head_base(it);
+    for (int base = 0; base < R * 8; base += n * kBatch) {
+      uint4 xl[kBatch], xh[kBatch];
+      int prow[kBatch];
+#pragma unroll
+      for (int bi = 0; bi < kBatch; ++bi) {
+        const int idx = base + t + n * bi;
+        if (idx < R * 8) {
+          const uint4* src = row_src(head0, idx >> 3, prow[bi]);
+          xl[bi] = src[idx & 7];
+          xh[bi] = src[(idx & 7) + 8];
+        }
+      }
+#pragma unroll
+      for (int bi = 0; bi < kBatch; ++bi) {
+        const int idx = base + t + n * bi;
+        if (idx >= R * 8) break;
+        const int r = idx >> 3, part = idx & 7;
+        const __nv_bfloat162* l2 = reinterpret_cast<const __nv_bfloat162*>(&xl[bi]);
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&xh[bi]);
+        uint4 o[4];  // slab 0 hi, slab 1 hi, slab 0 lo, slab 1 lo
+        __nv_bfloat162* o0 = reinterpret_cast<__nv_bfloat162*>(&o[0]);
+        __nv_bfloat162* o1 = reinterpret_cast<__nv_bfloat162*>(&o[1]);
+        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o[2]);
+        __nv_bfloat162* o3 = reinterpret_cast<__nv_bfloat162*>(&o[3]);
+        const float2* cs = P.rope + prow[bi] * kRopePairs + part * 8;  // shared by all units: L1-resident
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 a = __bfloat1622float2(l2[e]), bb = __bfloat1622float2(h2[e]);
+          const float2 c0 = __ldg(cs + 2 * e), c1 = __ldg(cs + 2 * e + 1);
+          const float2 vl =
+              make_float2((a.x * c0.x - bb.x * c0.y) * qk_scale, (a.y * c1.x - bb.y * c1.y) * qk_scale);
+          const float2 vh =
+              make_float2((bb.x * c0.x + a.x * c0.y) * qk_scale, (bb.y * c1.x + a.y * c1.y) * qk_scale);
+          o0[e] = __float22bfloat162_rn(vl);
+          o1[e] = __float22bfloat162_rn(vh);
+          const float2 fl = __bfloat1622float2(o0[e]), fh = __bfloat1622float2(o1[e]);
+          o2[e] = __floats2bfloat162_rn(vl.x - fl.x, vl.y - fl.y);
+          o3[e] = __floats2bfloat162_rn(vh.x - fh.x, vh.y - fh.y);
+        }
+        const uint32_t inrow = (uint32_t)r * 128 + (uint32_t)((part ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(q_hi + inrow) = o[0];
+        *reinterpret_cast<uint4*>(q_hi + slab_q + inrow) = o[1];
+        *reinterpret_cast<uint4*>(q_lo + inrow) = o[2];
+        *reinterpret_cast<uint4*>(q_lo + slab_q + inrow) = o[3];
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive(qready);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -480,166 +628,291 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       }
     }
   } else if (warp == 2) {
-    // ------------------------------------------------------------ row builder
-    const float qk_scale = kLog2e * rsqrtf((float)kD);  // rows carry 1/sqrt(d) and log2(e)
-    const uint32_t slab_q = (uint32_t)lay.qrows * 128;
-    for (int it = 0; it < mine; ++it) {
-      if (it > 0) {  // the previous unit's MMAs must be done with the row buffers
-        const bool ok = __all_sync(kFull, mbar_wait(qfree, (uint32_t)((it - 1) & 1), ctl, P.status));
+    if (P.compact) {
+      // ---------------------------------------------------------- in-place compaction
+      // BeaconKV reading notes §2.3 eq. 8: K_hat = K[:, I_final], V_hat = V[:, I_final].
+      // With the dropped slots d_0 < ... < d_{D-1}, the rows of run r,
+      // (d_r, d_{r+1}), move down by r + 1 slots; rows below d_0 stay. Each run
+      // goes through shared memory in chunks of kChunkRows rows with bulk
+      // copies, in increasing address order. A chunk's store overlaps only
+      // sources that were loaded before it (its own and earlier chunks'), and
+      // every later load reads above every earlier store's destination, so
+      // loads may run ahead of stores. One lane issues everything.
+      if (lane == 0) {
+        long long cg = 0;  // global chunk counter: buffer cg % cbufs, phase (cg / cbufs) & 1
+        const int CB = lay.cbufs, D = lay.D;
+        bool ok = true;
+        for (int it = 0; it < mine && ok; ++it) {
+          const int b = it & 1;
+          ok = mbar_wait(&dready[b], (uint32_t)((it >> 1) & 1), ctl, P.status);
+          if (!ok) break;
+          const int* dl = dlist + b * D;
+          int layer, seq, kvh;
+          unit_geom(blockIdx.x + it * gridDim.x, P.batch, P.kv_heads, layer, seq, kvh);
+          const size_t rowbase = (size_t)(seq * P.kv_heads + kvh) * P.max_cache;
+          char* tb[2] = {reinterpret_cast<char*>(P.Kc[layer] + rowbase * kD),
+                         reinterpret_cast<char*>(P.Vc[layer] + rowbase * kD)};
+          // chunk cursor: tensor t, run r, next source row
+          struct Cur {
+            int t, r, row;
+          };
+          auto start = [&](Cur& c) {
+            c.t = 0;
+            c.r = 0;
+            c.row = D > 0 ? dl[0] + 1 : L;
+          };
+          auto next = [&](Cur& c, int& t, int& src, int& n) -> bool {
+            while (c.t < 2 && D > 0) {
+              const int end = c.r + 1 < D ? dl[c.r + 1] : L;
+              if (c.row < end) {
+                n = end - c.row < kChunkRows ? end - c.row : kChunkRows;
+                t = c.t;
+                src = c.row;
+                c.row += n;
+                return true;
+              }
+              if (++c.r < D) {
+                c.row = dl[c.r] + 1;
+              } else {
+                ++c.t;
+                c.r = 0;
+                c.row = dl[0] + 1;
+              }
+            }
+            return false;
+          };
+          Cur lc, sc2;
+          start(lc);
+          start(sc2);
+          bulk_wait_read<0>();  // the previous unit's stores are done reading every chunk buffer
+          long long nl = 0, ns = 0;
+          int t, src, n;
+          while (nl < CB - 1 && next(lc, t, src, n)) {
+            const long long gi = cg + nl;
+            uint64_t* bar = &cfull[gi % CB];
+            mbar_expect_tx(bar, (uint32_t)(n * kD * 2));
+            bulk_load(smem_u32(cst + (gi % CB) * kChunkBytes), tb[t] + (size_t)src * kD * 2, (uint32_t)(n * kD * 2), bar);
+            ++nl;
+          }
+          while (ns < nl && ok) {
+            int st2, ssrc, sn;
+            next(sc2, st2, ssrc, sn);
+            const long long gi = cg + ns;
+            ok = mbar_wait(&cfull[gi % CB], (uint32_t)((gi / CB) & 1), ctl, P.status);
+            if (!ok) break;
+            const int shift = sc2.r + 1;  // run index of the chunk just taken, plus one
+            bulk_store(tb[st2] + (size_t)(ssrc - shift) * kD * 2, smem_u32(cst + (gi % CB) * kChunkBytes),
+                       (uint32_t)(sn * kD * 2));
+            bulk_commit();
+            ++ns;
+            if (next(lc, t, src, n)) {
+              bulk_wait_read<1>();  // the buffer of chunk ns - 2 (reused now) has been read out
+              const long long gl = cg + nl;
+              uint64_t* bar = &cfull[gl % CB];
+              mbar_expect_tx(bar, (uint32_t)(n * kD * 2));
+              bulk_load(smem_u32(cst + (gl % CB) * kChunkBytes), tb[t] + (size_t)src * kD * 2,
+                        (uint32_t)(n * kD * 2), bar);
+              ++nl;
+            }
+          }
+          if (!ok) {  // after an abort, loads already issued must land before the CTA exits
+            for (long long gi = cg + ns; gi < cg + nl; ++gi) {
+              const long long t0 = clock64();
+              while (!mbar_test(&cfull[gi % CB], (uint32_t)((gi / CB) & 1)) && clock64() - t0 < kWaitCycles) {
+              }
+            }
+          }
+          cg += nl;
+          if (ok && D > 0 && P.rows_moved)
+            atomicAdd(P.rows_moved, (unsigned long long)(L - D - dl[0]));
+          mbar_arrive(&dfree[b]);
+        }
+        bulk_wait_all();  // every store has landed before the CTA may exit
+      }
+    } else {
+      // ---------------------------------------------------------- L2 warmer
+      // Pulls the next unit's source rows into L2 while the current unit is
+      // scored, so the row build at the unit boundary reads from L2.
+      for (int it = 0; it + 1 < mine; ++it) {
+        const bool ok = __all_sync(kFull, mbar_wait(qready, (uint32_t)(it & 1), ctl, P.status));
         if (!ok) break;
-      }
-      int layer, seq, kvh;
-      unit_geom(blockIdx.x + it * gridDim.x, P.batch, P.kv_heads, layer, seq, kvh);
-      const int64_t head0 =
-          ((int64_t)layer * P.batch + seq) * (P.kv_heads * P.group) + (int64_t)kvh * P.group;
-      for (int idx = lane; idx < R * 8; idx += 32) {
-        const int r = idx >> 3, part = idx & 7;
-        const int gi = r / per_head, w = r % per_head;
-        const int64_t hq = head0 + gi;
-        const uint4* src;
-        int prow;
-        if (w < P.nb) {
-          src = P.bq + (hq * P.fps_cap + w) * 16;
-          prow = 0;
-        } else {
-          const int kq = w - P.nb;
-          src = P.rq + (hq * P.n_rq + (P.ring_first + kq) % P.n_rq) * 16;
-          prow = 1 + kq;
+        const int64_t h1 = head_base(it + 1);
+        for (int r = lane; r < R; r += 32) {
+          int pr;
+          const char* src = reinterpret_cast<const char*>(row_src(h1, r, pr));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128));
         }
-        const uint4 xl = src[part], xh = src[part + 8];
-        const __nv_bfloat162* l2 = reinterpret_cast<const __nv_bfloat162*>(&xl);
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&xh);
-        uint4 o[4];  // slab 0 hi, slab 1 hi, slab 0 lo, slab 1 lo
-        __nv_bfloat162* o0 = reinterpret_cast<__nv_bfloat162*>(&o[0]);
-        __nv_bfloat162* o1 = reinterpret_cast<__nv_bfloat162*>(&o[1]);
-        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o[2]);
-        __nv_bfloat162* o3 = reinterpret_cast<__nv_bfloat162*>(&o[3]);
-        const float2* cs = P.rope + prow * kRopePairs + part * 8;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 a = __bfloat1622float2(l2[e]), bb = __bfloat1622float2(h2[e]);
-          const float2 c0 = cs[2 * e], c1 = cs[2 * e + 1];
-          const float2 vl =
-              make_float2((a.x * c0.x - bb.x * c0.y) * qk_scale, (a.y * c1.x - bb.y * c1.y) * qk_scale);
-          const float2 vh =
-              make_float2((bb.x * c0.x + a.x * c0.y) * qk_scale, (bb.y * c1.x + a.y * c1.y) * qk_scale);
-          o0[e] = __float22bfloat162_rn(vl);
-          o1[e] = __float22bfloat162_rn(vh);
-          const float2 fl = __bfloat1622float2(o0[e]), fh = __bfloat1622float2(o1[e]);
-          o2[e] = __floats2bfloat162_rn(vl.x - fl.x, vl.y - fl.y);
-          o3[e] = __floats2bfloat162_rn(vh.x - fh.x, vh.y - fh.y);
-        }
-        const uint32_t inrow = (uint32_t)r * 128 + (uint32_t)((part ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(q_hi + inrow) = o[0];
-        *reinterpret_cast<uint4*>(q_hi + slab_q + inrow) = o[1];
-        *reinterpret_cast<uint4*>(q_lo + inrow) = o[2];
-        *reinterpret_cast<uint4*>(q_lo + slab_q + inrow) = o[3];
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(qready);
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------ keep-set selector
     for (int it = 0; it < mine; ++it) {
-      const int b = it & 1;
-      const bool ok = __all_sync(kFull, mbar_wait(&sready[b], (uint32_t)((it >> 1) & 1), ctl, P.status));
+      const int b = it % NSC, db = it & 1;
+      bool ok = __all_sync(kFull, mbar_wait(&sready[b], (uint32_t)((it / NSC) & 1), ctl, P.status));
+      // the copier must be done with this drop-list buffer (unit it - 2)
+      if (ok && P.compact && it >= 2)
+        ok = __all_sync(kFull, mbar_wait(&dfree[db], (uint32_t)(((it >> 1) + 1) & 1), ctl, P.status));
       if (!ok) break;
       const int u = blockIdx.x + it * gridDim.x;
       const float* s_u = sc + (size_t)b * lay.Lp;
       bool bad = false;
       for (int j = lane; j < L; j += 32) bad |= s_u[j] != s_u[j];
       if (__any_sync(kFull, bad) && lane == 0) latch(P.status, BKV_ERR_NONFINITE);
-      if (!select_keep(s_u, L, P.prefix, P.recent, P.budget, P.kept + (size_t)u * P.budget, hist) && lane == 0)
-        latch(P.status, BKV_ERR_INTERNAL);
+      select_keep(s_u, L, P.prefix, P.recent, P.budget, P.kept + (size_t)u * P.budget, dropbits,
+                  P.compact ? dlist + db * lay.D : nullptr);
       if (P.scores) {
         float* so = P.scores + (size_t)u * P.max_cache;
         for (int j = lane; j < L; j += 32) so[j] = s_u[j];
       }
       __syncwarp();
+      if (P.compact) mbar_arrive(&dready[db]);
       mbar_arrive(&sfree[b]);
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int et = tid - 128, q = warp - 4;
+    // Two warpgroups alternate over the TMEM buffers: group e takes the tiles
+    // with (global tile index & 1) == e. In pass 1 each keeps its own running
+    // (max, sum) per row; the two are merged into lse at the end of pass 1.
+    const int grp = (warp - 4) >> 2;
+    const int et = tid - 128 - grp * kEpiThreads, q = warp & 3;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const float neg_inf = __int_as_float(0xff800000u);
     long long g = 0;
     bool ok = true;
+    const int bt = tid - 128;  // 0..255 over both groups, for the row build
+    if (mine > 0) build_rows(0, bt, 2 * kEpiThreads);
     for (int it = 0; it < mine && ok; ++it) {
-      const int b_sc = it & 1;
+      const int b_sc = it % NSC;
       float* s_u = sc + (size_t)b_sc * lay.Lp;
       float run_m[2] = {neg_inf, neg_inf}, run_z[2] = {0.f, 0.f};
-      for (int s = 0; s < 2 * T; ++s, ++g) {
+      for (int s = 0; s < 2 * T && ok; ++s, ++g) {
         const int b = (int)(g & 1);
-        ok = __all_sync(kFull, mbar_wait(&tfull[b], (uint32_t)((g >> 1) & 1), ctl, P.status));
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t col0 = tmem + lane_base + (uint32_t)(b * lay.bufcols);
-        const int kt = s % T;
-        if (s < T) {
-          // pass 1: this thread owns observation row et (and et + 128 with a second M tile)
-          for (int mt = 0; mt < lay.mtiles; ++mt) {
-            const int row = mt ? lay.Rp16 - 128 + et : et;
-            if (mt && row < 128) continue;  // the second tile overlaps the first on these lanes
-            const int bound = lim[row] - kt * kTileKeys;  // keys [0, bound) are visible
+        if (b == grp) {
+          ok = __all_sync(kFull, mbar_wait(&tfull[b], (uint32_t)((g >> 1) & 1), ctl, P.status));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t col0 = tmem + lane_base + (uint32_t)(b * lay.bufcols);
+          const int kt = s % T;
+          if (s < T) {
+            // pass 1: this thread owns observation row et (and a row of the second M tile)
+            for (int mt = 0; mt < lay.mtiles; ++mt) {
+              const int row = mt ? lay.Rp16 - 128 + et : et;
+              if (mt && row < 128) continue;  // the second tile overlaps the first on these lanes
+              const int bound = lim[row] - kt * kTileKeys;  // keys [0, bound) are visible
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              float v[32];
-              tmem_ld32(col0 + (uint32_t)(mt * 128 + h * 32), v);
-              tmem_wait_ld();
-              if (bound < (h + 1) * 32) {
+              for (int h = 0; h < 4; h += 2) {
+                float v[64];
+                tmem_ld32(col0 + (uint32_t)(mt * 128 + h * 32), *reinterpret_cast<float(*)[32]>(&v[0]));
+                tmem_ld32(col0 + (uint32_t)(mt * 128 + h * 32 + 32), *reinterpret_cast<float(*)[32]>(&v[32]));
+                tmem_wait_ld();
+                if (bound < (h + 2) * 32) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  if (h * 32 + e >= bound) v[e] = neg_inf;
-              }
-              float tm = v[0];
+                  for (int e = 0; e < 64; ++e)
+                    if (h * 32 + e >= bound) v[e] = neg_inf;
+                }
+                float t0 = v[0], t1 = v[1], t2 = v[2], t3 = v[3];
 #pragma unroll
-              for (int e = 1; e < 32; ++e) tm = fmaxf(tm, v[e]);
-              const float nm = fmaxf(run_m[mt], tm);
-              if (nm != neg_inf) {
-                float z = run_m[mt] == neg_inf ? 0.f : run_z[mt] * fast_exp2(run_m[mt] - nm);
+                for (int e = 4; e < 64; e += 4) {
+                  t0 = fmaxf(t0, v[e]);
+                  t1 = fmaxf(t1, v[e + 1]);
+                  t2 = fmaxf(t2, v[e + 2]);
+                  t3 = fmaxf(t3, v[e + 3]);
+                }
+                const float nm = fmaxf(run_m[mt], fmaxf(fmaxf(t0, t1), fmaxf(t2, t3)));
+                if (nm != neg_inf) {
+                  float z0 = run_m[mt] == neg_inf ? 0.f : run_z[mt] * fast_exp2(run_m[mt] - nm);
+                  float z1 = 0.f, z2 = 0.f, z3 = 0.f;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) z += fast_exp2(v[e] - nm);
-                run_z[mt] = z;
-                run_m[mt] = nm;
+                  for (int e = 0; e < 64; e += 4) {
+                    z0 += fast_exp2(v[e] - nm);
+                    z1 += fast_exp2(v[e + 1] - nm);
+                    z2 += fast_exp2(v[e + 2] - nm);
+                    z3 += fast_exp2(v[e + 3] - nm);
+                  }
+                  run_z[mt] = (z0 + z1) + (z2 + z3);
+                  run_m[mt] = nm;
+                }
               }
             }
+          } else {
+            // pass 2: this thread owns key j of the tile; columns are observation rows
+            const int j = kt * kTileKeys + et;
+            const bool masked_tile = (kt + 1) * kTileKeys > L - P.nr + 1;
+            float m0 = neg_inf, m1 = neg_inf, m2 = neg_inf, m3 = neg_inf;
+            for (int c = 0; c < lay.Rp16; c += 64) {
+              float v[64];
+              tmem_ld32(col0 + (uint32_t)c, *reinterpret_cast<float(*)[32]>(&v[0]));
+              tmem_ld32(col0 + (uint32_t)c + 32, *reinterpret_cast<float(*)[32]>(&v[32]));  // inside the buffer
+              tmem_wait_ld();
+              if (!masked_tile && c + 64 <= R) {
+                const float4* l4 = reinterpret_cast<const float4*>(lse + c);
+#pragma unroll
+                for (int e = 0; e < 64; e += 4) {
+                  const float4 l = l4[e >> 2];
+                  m0 = fmaxf(m0, v[e] - l.x);
+                  m1 = fmaxf(m1, v[e + 1] - l.y);
+                  m2 = fmaxf(m2, v[e + 2] - l.z);
+                  m3 = fmaxf(m3, v[e + 3] - l.w);
+                }
+              } else {
+                // rows r >= R carry lim = 0, so the visibility test masks them too
+                const float4* l4 = reinterpret_cast<const float4*>(lse + c);
+                const int4* b4 = reinterpret_cast<const int4*>(lim + c);
+#pragma unroll
+                for (int e = 0; e < 64; e += 4) {
+                  const float4 l = l4[e >> 2];
+                  const int4 bd = b4[e >> 2];
+                  m0 = fmaxf(m0, j < bd.x ? v[e] - l.x : neg_inf);
+                  m1 = fmaxf(m1, j < bd.y ? v[e + 1] - l.y : neg_inf);
+                  m2 = fmaxf(m2, j < bd.z ? v[e + 2] - l.z : neg_inf);
+                  m3 = fmaxf(m3, j < bd.w ? v[e + 3] - l.w : neg_inf);
+                }
+              }
+            }
+            const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+            if (j < L) s_u[j] = mx == neg_inf ? 0.f : fast_exp2(mx);
           }
           tc_fence_before();
           mbar_arrive(&tempty[b]);
-          if (s == T - 1) {
+        }
+        if (s == T - 1) {
+          // merge the two groups' row statistics into lse
+          for (int mt = 0; mt < lay.mtiles; ++mt) {
+            const int row = mt ? lay.Rp16 - 128 + et : et;
+            if (mt && row < 128) continue;
+            pm[grp * lay.qrows + row] = run_m[mt];
+            pz[grp * lay.qrows + row] = run_z[mt];
+          }
+          mbar_arrive(lsebar);
+          ok = __all_sync(kFull, mbar_wait(lsebar, (uint32_t)(it & 1), ctl, P.status));
+          if (!ok) break;
+          if (grp == 0) {
             for (int mt = 0; mt < lay.mtiles; ++mt) {
               const int row = mt ? lay.Rp16 - 128 + et : et;
               if (mt && row < 128) continue;
-              lse[row] = run_z[mt] > 0.f ? run_m[mt] + fast_log2(run_z[mt]) : neg_inf;
-            }
-            mbar_arrive(lsebar);  // every row's lse is needed by every key in pass 2
-            ok = __all_sync(kFull, mbar_wait(lsebar, (uint32_t)(it & 1), ctl, P.status));
-            // this unit's scores go to sc[b_sc]: the selector must be done with unit it - 2
-            if (ok && it >= 2)
-              ok = __all_sync(kFull, mbar_wait(&sfree[b_sc], (uint32_t)(((it >> 1) + 1) & 1), ctl, P.status));
-            if (!ok) break;
-          }
-        } else {
-          // pass 2: this thread owns key j of the tile; columns are observation rows
-          const int j = kt * kTileKeys + et;
-          const bool masked_tile = (kt + 1) * kTileKeys > L - P.nr + 1;
-          float mx = neg_inf;
-          for (int c = 0; c < lay.Rp16; c += 32) {
-            float v[32];
-            tmem_ld32(col0 + (uint32_t)c, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int r = c + e;
-              if (r < R && (!masked_tile || j < lim[r])) mx = fmaxf(mx, v[e] - lse[r]);
+              const float ma = pm[row], mb = pm[lay.qrows + row];
+              const float mm = fmaxf(ma, mb);
+              float zz = 0.f;
+              if (mm != neg_inf)
+                zz = (ma == neg_inf ? 0.f : pz[row] * fast_exp2(ma - mm)) +
+                     (mb == neg_inf ? 0.f : pz[lay.qrows + row] * fast_exp2(mb - mm));
+              lse[row] = zz > 0.f ? mm + fast_log2(zz) : neg_inf;
             }
           }
-          tc_fence_before();
-          mbar_arrive(&tempty[b]);
-          if (j < L) s_u[j] = mx == neg_inf ? 0.f : fast_exp2(mx);
-          if (s == 2 * T - 1) mbar_arrive(&sready[b_sc]);
+          mbar_arrive(lse2bar);
+          ok = __all_sync(kFull, mbar_wait(lse2bar, (uint32_t)(it & 1), ctl, P.status));
+          // this unit's scores go to sc[b_sc]: the selector must be done with unit it - NSC
+          if (ok && it >= NSC)
+            ok = __all_sync(kFull, mbar_wait(&sfree[b_sc], (uint32_t)(((it / NSC) + 1) & 1), ctl, P.status));
+          if (!ok) break;
         }
+        if (s == 2 * T - 1) mbar_arrive(&sready[b_sc]);
+      }
+      // rows of the next unit: the MMAs of this one must be done with the buffers
+      if (ok && it + 1 < mine) {
+        ok = __all_sync(kFull, mbar_wait(qfree, (uint32_t)(it & 1), ctl, P.status));
+        if (ok) build_rows(it + 1, bt, 2 * kEpiThreads);
       }
     }
   }
@@ -651,9 +924,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   if (warp == 1) tmem_dealloc(tmem, ncols);
 }
 
-size_t score_smem_bytes(int R, int L) {
-  const Layout s = make_layout(R, L);
-  return s.stages >= 2 ? s.total : (size_t)1 << 30;  // under two stages: not supported
+size_t score_smem_bytes(int R, int L, int nr, int budget, int compact) {
+  const Layout s = make_layout(R, L, nr, budget, compact);
+  return s.stages >= 2 ? s.total : (size_t)1 << 30;  // no plan fits: not supported
 }
 
 bool encode_kmaps(ScoreParams& p, const void* const* K, int layers, int batch, int kv_heads,
@@ -684,7 +957,7 @@ bool encode_kmaps(ScoreParams& p, const void* const* K, int layers, int batch, i
 }
 
 cudaError_t launch_score_select(const ScoreParams& p, cudaStream_t s) {
-  const size_t smem = score_smem_bytes(p.group * (p.nb + p.nr), p.L);
+  const size_t smem = score_smem_bytes(p.group * (p.nb + p.nr), p.L, p.nr, p.budget, p.compact);
   static size_t configured = 0;
   if (smem > configured) {
     const cudaError_t e =

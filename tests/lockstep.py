@@ -89,6 +89,10 @@ def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "c
     oracles = {u: UnitOracle(G, d, w.theta, w.budget, w.prefix, w.recent, w.fps_cap, w.fps_keep)
                for u in sample_units}
     live = set(sample_units)
+    idx_dev = torch.device(gen_device)
+    l_idx = torch.tensor([u[0] for u in sample_units], device=idx_dev)
+    b_idx = torch.tensor([u[1] for u in sample_units], device=idx_dev)
+    kh_idx = torch.tensor([u[2] for u in sample_units], device=idx_dev)
     rep = LockstepReport()
     n_rq = w.fps_cap - w.fps_keep
 
@@ -108,11 +112,14 @@ def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "c
                 K[l][:, :, cache_len] = kd[l]
                 V[l][:, :, cache_len] = vd[l]
             bkv.bkv_append_queries(h, qd, t)
-            qb, kb, vb = to_bits(q), to_bits(k), to_bits(v)
-            for (l, b, kh) in sample_units:
+            # only the sampled units' rows travel to the host
+            qs = to_bits(q[l_idx, b_idx])            # [units][heads][d]
+            ks = to_bits(k[l_idx, b_idx, kh_idx])    # [units][d]
+            vs = to_bits(v[l_idx, b_idx, kh_idx])
+            for i, (l, b, kh) in enumerate(sample_units):
                 uo = oracles[(l, b, kh)]
-                uo.append_kv(kb[l, b, kh], vb[l, b, kh], t)
-                uo.append_queries(qb[l, b, kh * G:(kh + 1) * G], t)
+                uo.append_kv(ks[i], vs[i], t)
+                uo.append_queries(qs[i, kh * G:(kh + 1) * G], t)
             cache_len += 1
             if cache_len < w.budget + w.period:
                 continue

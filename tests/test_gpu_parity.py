@@ -72,6 +72,19 @@ def test_qwen3_4b_b1_first_eviction_sampled_units():
     assert rep.units_checked == len(units) * rep.evictions
 
 
+def test_qwen3_4b_b192_full_size_sampled_units():
+    """The benchmark workload at full size (58 GB of K/V, 55,296 units, the
+    bench's launch configuration), checked on sampled units over three
+    evictions, inputs generated on the device."""
+    w = WORKLOADS["qwen3_4b_b192"]
+    units = [(0, 0, 0), (3, 191, 7), (11, 64, 2), (17, 100, 5), (24, 17, 3), (35, 150, 6),
+             (35, 191, 0), (8, 1, 1)]
+    rep = run_lockstep(w, seed=0xBEAC2, sample_units=units, gen_device="cuda",
+                       steps=w.max_cache + 2 * w.period)
+    assert_clean(rep, min_evictions=3)
+    assert rep.units_checked == len(units) * rep.evictions
+
+
 def wide_queries(t, q):
     """Replaces some queries by vectors whose exponents span far more than 20
     binades (FPS's wide exact-sum path), by zero rows and by exact duplicates."""
