@@ -54,7 +54,7 @@ struct FpsParams {
   uint32_t* status;
   int64_t heads_total;
   int fps_cap, n_rq;
-  int nb, nr;               // candidates: nb beacons then nr recents (N = nb + nr <= 32)
+  int nb, nr;               // candidates: nb beacons then nr recents (N = nb + nr <= 64)
   int ring_first;           // ring slot of the oldest recent
   int m;                    // rows kept (fps_keep)
 };

@@ -1,4 +1,4 @@
-// Farthest-point sampling of pre-RoPE queries, one CTA per query head.
+// Farthest-point sampling of pre-RoPE queries, one warp per query head.
 //
 // BeaconKV reading notes, §2.2, Algorithm 1 (and eq. 9 / Algorithm 2 for when
 // it runs): with cos the cosine similarity of two candidates,
@@ -13,12 +13,18 @@
 // zero), a_i is summed left to right in j order and then divided by N. Every
 // pick this kernel makes is the pick that arithmetic makes, bit for bit, but
 // float64 runs only where it can change the answer:
-//   * the Gram matrix is first formed in float32 from the bf16 rows scaled by a
-//     power of two (exact), with four interleaved partial sums; products of
-//     bf16 values are exact in float32, so the Gram error is at most
-//     gamma_33 * ||x_i|| ||x_j|| (plus < 2^-142 from products that underflow)
-//     and the float32 cosine c_ij is within kCosErr = 2e-5 of the float64
-//     cosine (the derived bound is 4.7e-6);
+//   * each row is scaled by a power of two that brings its largest component
+//     into [1, 4), or above 2^-7 for a row of bf16 subnormals (exact, apart
+//     from components more than ~120 binades below the largest, which may
+//     round in the float32 subnormal range);
+//   * the float32 Gram entry is two interleaved sums (even and odd k) of 64
+//     exact bf16 products each, added once, so its error is at most
+//     gamma_64 * ||y_i|| ||y_j|| (3.8e-6 relative) plus < 2^-140 from
+//     subnormal rounding, against ||y_i|| >= 2^-7 for every nonzero row;
+//   * c_ij = (G32_ij * r_i) * r_j with r_i = rsqrtf(G32_ii) (2 ulp) is then
+//     within 8.5e-6 of the float64 cosine; the filters use kCosErr = 2e-5;
+//   * the mean a_i in float32 (any summation order, N <= 64) is within
+//     8.5e-6 + 63 * 2^-24 of the float64 mean; the filters use kMeanErr;
 //   * a decision (argmin of the mean cosine, argmin of the running max) is
 //     final when the float32 minimum beats every other candidate by more than
 //     twice its error bound - then the float64 values order the same way;
@@ -27,7 +33,10 @@
 // The exact G_ij uses 64-bit integer arithmetic on the bf16 significands when
 // both vectors' exponents span <= 20 binades (128 products then sum below
 // 2^63), otherwise a 544-bit fixed-point accumulator over the whole bf16
-// product range; either way it is rounded once to nearest even.
+// product range; either way it is rounded once to nearest even. The per-row
+// data the exact path needs (exponent range, exact G_ii) is computed only when
+// a head meets its first close call.
+#include <atomic>
 #include <climits>
 
 #include "bkv_internal.cuh"
@@ -36,57 +45,51 @@ namespace bkv {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kHeadsPerCta = 2;       // one warp per head
 constexpr int kMaxCand = 64;          // beacons (< fps_cap <= 32) + recents (<= 32)
-constexpr int kYStride = kD + 4;      // float row stride (528 B): LDS.128 rows hit distinct banks
+constexpr int kYStride = kD + 4;      // float row stride: LDS.128 of 8 consecutive rows hit distinct banks
 constexpr float kCosErr = 2e-5f;      // |c32 - cos64| bound used by the filters
-constexpr float kMeanErr = 2.5e-5f;   // |a32 - a64| bound (kCosErr + summation error, N <= 64)
+constexpr float kMeanErr = 2.5e-5f;   // |a32 - a64| bound used by the filters
+constexpr unsigned kFull = 0xFFFFFFFFu;
 
-// Dynamic shared memory for n candidates.
-struct FpsSmem {
-  uint4* x;        // [n][16]   bf16 rows
-  float* y;        // [n][kYStride] rows scaled by 2^-(emax+8), exact in float32
-  float* c;        // [n][n+1]  float32 cosines
-  double* diag;    // [n]       exact G_ii rounded to float64
-  int* emin;       // [n]       smallest exponent of a nonzero component
-  int* emax;       // [n]
-  int* flags;      // [n]       bit 0: wide (exponent span > 20), bit 1: y not exact
-  int* picks;      // [32]      pick order
-  int* keep_src;   // [32]
-  int* cand;       // [kMaxCand] fallback candidate list
-  double* v64;     // [kMaxCand] fallback values
-  int n;
-  __device__ float& Y(int i, int k) { return y[i * kYStride + k]; }
-  __device__ float& C(int i, int j) { return c[i * (n + 1) + j]; }
+// Per-warp shared memory for NT = 32 * NH candidate slots.
+template <int NH>
+struct WarpSmem {
+  static constexpr int NT = 32 * NH;
+  static constexpr size_t kY = (size_t)NT * kYStride * 4;
+  // NH == 1: the cosine matrix reuses the rows' space once the Gram is in registers
+  static constexpr size_t kC = NH == 1 ? 0 : (((size_t)NT * (NT + 1) * 4 + 15) / 16) * 16;
+  static constexpr size_t kMisc = (size_t)NT * 8 * 2 + (size_t)NT * 4 * 5 + 64 * 4;
+  static constexpr size_t kBytes = ((kY + kC + kMisc) + 15) / 16 * 16;
+
+  float* y;       // [NT][kYStride] rows scaled by a power of two, float32
+  float* c;       // [NT][NT + 1]   Gram, then cosines
+  double* diag;   // [NT] exact G_ii rounded to float64 (close calls only)
+  double* v64;    // [NT] exact values of a close call
+  float* inv;     // [NT] rsqrt of the float32 diagonal
+  int* emin;      // [NT] smallest exponent of a nonzero component
+  int* emax;      // [NT]
+  int* wide;      // [NT] exponent span > 20
+  int* cand;      // [NT] close-call candidates
+  int* picks;     // [32] pick order
+  int* keep_src;  // [32]
+
+  __device__ WarpSmem(unsigned char* base) {
+    y = reinterpret_cast<float*>(base);
+    c = NH == 1 ? y : reinterpret_cast<float*>(base + kY);
+    unsigned char* m = base + kY + kC;
+    diag = reinterpret_cast<double*>(m);
+    v64 = diag + NT;
+    inv = reinterpret_cast<float*>(v64 + NT);
+    emin = reinterpret_cast<int*>(inv + NT);
+    emax = emin + NT;
+    wide = emax + NT;
+    cand = wide + NT;
+    picks = cand + NT;
+    keep_src = picks + 32;
+  }
+  __device__ float& C(int i, int j) { return c[i * (NT + 1) + j]; }
 };
-
-__host__ __device__ inline size_t fps_smem_bytes(int n) {
-  return (size_t)n * 256 + (size_t)n * kYStride * 4 + (((size_t)n * (n + 1) * 4 + 15) / 16) * 16 +
-         (size_t)n * 8 + (size_t)n * 12 + 64 * 4 + (size_t)kMaxCand * 4 + (size_t)kMaxCand * 8 + 64;
-}
-
-__device__ inline FpsSmem carve(unsigned char* base, int n) {
-  FpsSmem s;
-  s.n = n;
-  size_t off = 0;
-  s.x = reinterpret_cast<uint4*>(base);
-  off += (size_t)n * 256;
-  s.y = reinterpret_cast<float*>(base + off);
-  off += (size_t)n * kYStride * 4;
-  s.c = reinterpret_cast<float*>(base + off);
-  off += (((size_t)n * (n + 1) * 4 + 15) / 16) * 16;
-  s.diag = reinterpret_cast<double*>(base + off);
-  off += (size_t)n * 8;
-  s.v64 = reinterpret_cast<double*>(base + off);
-  off += (size_t)kMaxCand * 8;
-  s.emin = reinterpret_cast<int*>(base + off);
-  s.emax = s.emin + n;
-  s.flags = s.emax + n;
-  s.picks = s.flags + n;
-  s.keep_src = s.picks + 32;
-  s.cand = s.keep_src + 32;
-  return s;
-}
 
 // bf16 = (-1)^neg * sig * 2^exp with an integer significand sig < 256.
 __device__ __forceinline__ void decode_bf16(uint32_t bits, int& sig, int& exp, int& neg,
@@ -184,73 +187,67 @@ __device__ __noinline__ double exact_dot_wide(const uint4* xa, const uint4* xb) 
   return negative ? -r : r;
 }
 
-// Exact dot product of rows i and j of the candidate set, rounded once to float64.
-__device__ double exact_dot(FpsSmem& sm, int i, int j) {
-  if ((sm.flags[i] | sm.flags[j]) & 1) return exact_dot_wide(sm.x + i * 16, sm.x + j * 16);
-  const int ei = sm.emin[i], ej = sm.emin[j];
+// Exact dot product of two bf16 rows, rounded once to float64; emin_* are the
+// rows' smallest nonzero exponents (used when neither row is wide).
+__device__ double exact_dot(const uint4* xi, const uint4* xj, int emin_i, int emin_j, bool wide) {
+  if (wide) return exact_dot_wide(xi, xj);
   long long acc = 0;
   for (int k = 0; k < kD; ++k) {
     int sa, ea, na, fa, sb, eb, nbv, fb;
-    decode_bf16(elem(sm.x + i * 16, k), sa, ea, na, fa);
-    decode_bf16(elem(sm.x + j * 16, k), sb, eb, nbv, fb);
+    decode_bf16(elem(xi, k), sa, ea, na, fa);
+    decode_bf16(elem(xj, k), sb, eb, nbv, fb);
     if (sa == 0 || sb == 0 || fa || fb) continue;
-    const long long p = (long long)(sa << (ea - ei)) * (long long)(sb << (eb - ej));
+    const long long p = (long long)(sa << (ea - emin_i)) * (long long)(sb << (eb - emin_j));
     acc += (na ^ nbv) ? -p : p;
   }
-  return acc == 0 ? 0.0 : __dmul_rn(__ll2double_rn(acc), pow2(ei + ej));
-}
-
-// The float64 cosine of the reference arithmetic.
-__device__ double cos64(FpsSmem& sm, int i, int j) {
-  const double gii = sm.diag[i], gjj = sm.diag[j];
-  if (gii == 0.0 || gjj == 0.0) return 0.0;
-  return __ddiv_rn(exact_dot(sm, i, j), __dsqrt_rn(__dmul_rn(gii, gjj)));
-}
-
-__device__ __forceinline__ float warp_min(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v = fminf(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
-  return v;
+  return acc == 0 ? 0.0 : __dmul_rn(__ll2double_rn(acc), pow2(emin_i + emin_j));
 }
 
 __device__ __forceinline__ double warp_max64(double v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
-    const double o = __shfl_xor_sync(0xFFFFFFFFu, v, off);
+    const double o = __shfl_xor_sync(kFull, v, off);
     v = o > v ? o : v;
   }
   return v;
 }
 
+// Order-preserving map of float32 to uint32 (for a single-instruction warp min).
+__device__ __forceinline__ uint32_t fkey(float v) {
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float unkey(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // Decides argmin over the candidates whose float32 values v0 (index lane) and
 // v1 (index lane + 32) are valid, with error bound err. Exact float64 values
 // for close candidates come from exact(j), evaluated cooperatively by the
-// warp: exact(j, lane) returns lane's share, combined with `combine`.
-// Returns the winning index (same on every lane).
+// warp (same value on every lane). Returns the winning index on every lane.
 template <class Exact>
-__device__ int filtered_argmin(FpsSmem& sm, float v0, float v1, bool ok0, bool ok1, float err,
-                               Exact exact) {
+__device__ int filtered_argmin(int* cand, float v0, float v1, bool ok0, bool ok1, float err, Exact exact) {
   const int lane = threadIdx.x & 31;
-  const float inf = __int_as_float(0x7f800000);
-  const float m = warp_min(fminf(ok0 ? v0 : inf, ok1 ? v1 : inf));
+  const uint32_t k = min(ok0 ? fkey(v0) : 0xFFFFFFFFu, ok1 ? fkey(v1) : 0xFFFFFFFFu);
+  const float m = unkey(__reduce_min_sync(kFull, k));
   const float lim = m + 2.0f * err;
-  const unsigned b0 = __ballot_sync(0xFFFFFFFFu, ok0 && v0 <= lim);
-  const unsigned b1 = __ballot_sync(0xFFFFFFFFu, ok1 && v1 <= lim);
+  const unsigned b0 = __ballot_sync(kFull, ok0 && v0 <= lim);
+  const unsigned b1 = __ballot_sync(kFull, ok1 && v1 <= lim);
   const int nc = __popc(b0) + __popc(b1);
   if (nc == 1) return b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
   if (nc == 0) {  // only with NaN values (already latched as non-finite): lowest valid index
-    const unsigned o0 = __ballot_sync(0xFFFFFFFFu, ok0), o1 = __ballot_sync(0xFFFFFFFFu, ok1);
+    const unsigned o0 = __ballot_sync(kFull, ok0), o1 = __ballot_sync(kFull, ok1);
     return o0 ? __ffs(o0) - 1 : (o1 ? 32 + __ffs(o1) - 1 : 0);
   }
   // close call: list the candidates in index order, then compare float64 values
-  if (ok0 && v0 <= lim) sm.cand[__popc(b0 & ((1u << lane) - 1u))] = lane;
-  if (ok1 && v1 <= lim) sm.cand[__popc(b0) + __popc(b1 & ((1u << lane) - 1u))] = lane + 32;
+  if (ok0 && v0 <= lim) cand[__popc(b0 & ((1u << lane) - 1u))] = lane;
+  if (ok1 && v1 <= lim) cand[__popc(b0) + __popc(b1 & ((1u << lane) - 1u))] = lane + 32;
   __syncwarp();
   int best = -1;
   double bv = 0.0;
   for (int q = 0; q < nc; ++q) {
-    const int j = sm.cand[q];
-    const double v = exact(j);  // warp-cooperative, same value on every lane
+    const int j = cand[q];
+    const double v = exact(j);
     if (best < 0 || v < bv) {
       best = j;
       bv = v;
@@ -260,169 +257,184 @@ __device__ int filtered_argmin(FpsSmem& sm, float v0, float v1, bool ok0, bool o
   return best;
 }
 
-__global__ void __launch_bounds__(kThreads) fps_kernel(FpsParams P) {
+template <int NH>
+__global__ void __launch_bounds__(32 * kHeadsPerCta) fps_kernel(FpsParams P) {
+  using W = WarpSmem<NH>;
+  constexpr int NT = W::NT;
   extern __shared__ __align__(16) unsigned char fps_smem[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t head = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t head = (int64_t)blockIdx.x * kHeadsPerCta + warp;
+  if (head >= P.heads_total) return;
   const int nb = P.nb, n = P.nb + P.nr, m = P.m;
-  if (m == 0) return;  // nothing is kept and there is no trace
-  FpsSmem sm = carve(fps_smem, n);
+  W sm(fps_smem + (size_t)warp * W::kBytes);
   uint4* bq = P.bq + head * P.fps_cap * 16;
   const uint4* rq = P.rq + head * P.n_rq * 16;
-
   // candidates: beacons (oldest first), then recents (oldest first)
-  for (int idx = tid; idx < n * 16; idx += kThreads) {
-    const int r = idx >> 4, part = idx & 15;
-    const uint4* src = r < nb ? bq + r * 16 : rq + ((P.ring_first + r - nb) % P.n_rq) * 16;
-    sm.x[idx] = src[part];
-  }
-  __syncthreads();
-
+  auto row = [&](int i) -> const uint4* {
+    return i < nb ? bq + i * 16 : rq + ((P.ring_first + i - nb) % P.n_rq) * 16;
+  };
   int8_t* trace = P.trace + head * m;
-  if (n <= m) {  // nothing to sample: keep every candidate in order
-    for (int idx = tid; idx < n * 16; idx += kThreads) bq[idx] = sm.x[idx];
-    for (int k = tid; k < m; k += kThreads) trace[k] = k < n ? (int8_t)k : (int8_t)-1;
-    return;
-  }
 
-  // per row: exponent range, scaled float32 copy, exact diagonal (4 threads per row)
-  for (int r0 = 0; r0 < n; r0 += kThreads / 4) {
-    const int r = r0 + (tid >> 2), q = tid & 3;
-    int emin = INT_MAX, emax = INT_MIN, bad = 0;
-    if (r < n) {
-      for (int k = q * 32; k < q * 32 + 32; ++k) {
-        int sig, e, neg, nf;
-        decode_bf16(elem(sm.x + r * 16, k), sig, e, neg, nf);
-        bad |= nf;
-        if (sig != 0 && !nf) {
-          emin = min(emin, e);
-          emax = max(emax, e);
-        }
-      }
-    }
+  if (n > m) {
+    // ---- rows -> float32, each scaled so its largest component lies in [1, 4)
+    // lanes 0-15 take one row, lanes 16-31 the next; padding rows are zero
+    bool bad = false;
+    for (int r0 = 0; r0 < NT; r0 += 2) {
+      const int r = r0 + (lane >> 4), part = lane & 15;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < n) v = __ldg(row(r) + part);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t e = 0;
 #pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-      emin = min(emin, __shfl_xor_sync(0xFFFFFFFFu, emin, off));
-      emax = max(emax, __shfl_xor_sync(0xFFFFFFFFu, emax, off));
-      bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, off);
-    }
-    const bool zero_row = emin == INT_MAX;
-    if (zero_row) emin = emax = 0;
-    const bool wide = (emax - emin) > 20;
-    const bool inexact = (emax - emin) > 110;  // scaled float32 copy could underflow
-    long long acc = 0;
-    if (r < n) {
-      if (bad && q == 0) latch(P.status, BKV_ERR_NONFINITE);
-      for (int k = q * 32; k < q * 32 + 32; ++k) {
-        int sig, e, neg, nf;
-        decode_bf16(elem(sm.x + r * 16, k), sig, e, neg, nf);
-        float yv = 0.f;
-        if (sig != 0 && !nf) {
-          // sig * 2^(e - emax - 8), exact: the power of two is a normal float32 here
-          if (!inexact) yv = (float)sig * __int_as_float((e - emax - 8 + 127) << 23);
-          if (!wide) acc += (long long)(sig << (e - emin)) * (long long)(sig << (e - emin));
-        }
-        sm.Y(r, k) = neg ? -yv : yv;
-      }
-    }
+      for (int q = 0; q < 4; ++q) e = max(e, max((w[q] >> 7) & 0xFFu, (w[q] >> 23) & 0xFFu));
 #pragma unroll
-    for (int off = 1; off < 4; off <<= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-    if (r < n && q == 0) {
-      sm.emin[r] = emin;
-      sm.emax[r] = emax;
-      sm.flags[r] = (wide ? 1 : 0) | (inexact ? 2 : 0);
-      if (!wide) sm.diag[r] = acc == 0 ? 0.0 : __dmul_rn(__ll2double_rn(acc), pow2(2 * emin));
+      for (int off = 1; off < 16; off <<= 1) e = max(e, __shfl_xor_sync(kFull, e, off));
+      bad |= e == 0xFFu;
+      const float scale = __int_as_float(max(254 - (int)e, 1) << 23);  // 2^(127 - e)
+      float f[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        f[2 * q] = __fmul_rn(__uint_as_float(w[q] << 16), scale);
+        f[2 * q + 1] = __fmul_rn(__uint_as_float(w[q] & 0xFFFF0000u), scale);
+      }
+      float4* dst = reinterpret_cast<float4*>(sm.y + r * kYStride + part * 8);
+      dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+      dst[1] = make_float4(f[4], f[5], f[6], f[7]);
     }
-  }
-  __syncthreads();
-  for (int r = tid; r < n; r += kThreads)  // wide rows: exact diagonal by the long accumulator
-    if (sm.flags[r] & 1) sm.diag[r] = exact_dot_wide(sm.x + r * 16, sm.x + r * 16);
-  __syncthreads();
+    if (__any_sync(kFull, bad) && lane == 0) latch(P.status, BKV_ERR_NONFINITE);
+    __syncwarp();
 
-  // float32 Gram: warp item = 8 rows x 32 columns; lane = column, rows broadcast
-  const int rblocks = (n + 7) / 8, cgroups = (n + 31) / 32;
-  for (int item = warp; item < rblocks * cgroups; item += kThreads / 32) {
-    const int i0 = (item % rblocks) * 8, j = (item / rblocks) * 32 + lane;
-    float s[8][4];
+    // ---- float32 Gram, 32 x 32 tiles; lane (I, J) = (lane & 7, lane >> 3)
+    // owns rows I + 8a (a < 4) and columns J + 4b (b < 8) of a tile, so each
+    // LDS.128 touches 8 (or 4) consecutive rows: distinct banks
+    const int I = lane & 7, J = lane >> 3;
+#pragma unroll 1
+    for (int tile = 0; tile < (NH == 1 ? 1 : 3); ++tile) {
+      const int ti = tile == 2 ? 1 : 0, tj = tile == 0 ? 0 : 1;
+      const float* ya = sm.y + (ti * 32 + I) * kYStride;
+      const float* yb = sm.y + (tj * 32 + J) * kYStride;
+      float2 s[4][8];
 #pragma unroll
-    for (int a = 0; a < 8; ++a) s[a][0] = s[a][1] = s[a][2] = s[a][3] = 0.f;
-    const float* yj = &sm.Y(j < n ? j : 0, 0);
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) s[a][b] = make_float2(0.f, 0.f);
 #pragma unroll 2
-    for (int k = 0; k < kD; k += 4) {
-      const float4 b = *reinterpret_cast<const float4*>(yj + k);
+      for (int k = 0; k < kD; k += 4) {
+        float4 av[4], bv[8];
 #pragma unroll
-      for (int a = 0; a < 8; ++a) {
-        const int i = i0 + a < n ? i0 + a : 0;
-        const float4 av = *reinterpret_cast<const float4*>(&sm.Y(i, k));
-        s[a][0] = __fmaf_rn(av.x, b.x, s[a][0]);
-        s[a][1] = __fmaf_rn(av.y, b.y, s[a][1]);
-        s[a][2] = __fmaf_rn(av.z, b.z, s[a][2]);
-        s[a][3] = __fmaf_rn(av.w, b.w, s[a][3]);
+        for (int a = 0; a < 4; ++a) av[a] = *reinterpret_cast<const float4*>(ya + 8 * a * kYStride + k);
+#pragma unroll
+        for (int b = 0; b < 8; ++b) bv[b] = *reinterpret_cast<const float4*>(yb + 4 * b * kYStride + k);
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            // (even k, odd k) partial sums of the same entry
+            s[a][b] = __ffma2_rn(make_float2(av[a].x, av[a].y), make_float2(bv[b].x, bv[b].y), s[a][b]);
+            s[a][b] = __ffma2_rn(make_float2(av[a].z, av[a].w), make_float2(bv[b].z, bv[b].w), s[a][b]);
+          }
       }
-    }
-    if (j < n) {
+      __syncwarp();  // with NH == 1 the Gram overwrites the rows every lane has finished reading
 #pragma unroll
-      for (int a = 0; a < 8; ++a)
-        if (i0 + a < n) sm.C(i0 + a, j) = __fadd_rn(__fadd_rn(s[a][0], s[a][1]), __fadd_rn(s[a][2], s[a][3]));
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          const int i = ti * 32 + I + 8 * a, j = tj * 32 + J + 4 * b;
+          const float g = __fadd_rn(s[a][b].x, s[a][b].y);
+          sm.C(i, j) = g;
+          if (ti != tj) sm.C(j, i) = g;  // exact products: the transposed sum is the same
+        }
     }
-  }
-  __syncthreads();
+    __syncwarp();
 
-  // float32 cosines, in place (each entry is read and rewritten by one thread);
-  // rows whose scaled copy is not exact take the float64 value
-  float* inv = reinterpret_cast<float*>(sm.v64);  // 1 / sqrt(G32_ii), reusing the fallback buffer
-  for (int i = tid; i < n; i += kThreads) inv[i] = sm.C(i, i) > 0.f ? rsqrtf(sm.C(i, i)) : 0.f;
-  __syncthreads();
-  for (int i = warp; i < n; i += kThreads / 32) {
-    for (int j = lane; j < n; j += 32) {
-      float v;
-      if ((sm.flags[i] | sm.flags[j]) & 2) v = __double2float_rn(cos64(sm, i, j));
-      else v = __fmul_rn(__fmul_rn(sm.C(i, j), inv[i]), inv[j]);
-      sm.C(i, j) = v;
+    // ---- cosines, row i by lane i (and i + 32), with the row sums for the means
+    for (int i = lane; i < NT; i += 32) {
+      const float g = sm.C(i, i);
+      sm.inv[i] = g > 0.f ? rsqrtf(g) : 0.f;
     }
-  }
-  __syncthreads();
+    __syncwarp();
+    float a[NH];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      const int i = lane + 32 * h;
+      float acc0 = 0.f, acc1 = 0.f;
+      if (i < n) {
+        const float ri = sm.inv[i];
+        for (int j = 0; j < n; ++j) {
+          const float v = __fmul_rn(__fmul_rn(sm.C(i, j), ri), sm.inv[j]);
+          sm.C(i, j) = v;
+          if (j & 1) acc1 = __fadd_rn(acc1, v);
+          else acc0 = __fadd_rn(acc0, v);
+        }
+      }
+      a[h] = __fdiv_rn(__fadd_rn(acc0, acc1), (float)n);
+    }
+    __syncwarp();
 
-  if (warp == 0) {
+    // ---- exact path, prepared on the first close call of this head
+    bool meta_ok = false;
+    auto meta = [&]() {
+      if (meta_ok) return;
+      for (int r = lane; r < n; r += 32) {
+        const uint4* x = row(r);
+        int emin = INT_MAX, emax = INT_MIN;
+        for (int k = 0; k < kD; ++k) {
+          int sig, e, neg, nf;
+          decode_bf16(elem(x, k), sig, e, neg, nf);
+          if (sig != 0 && !nf) {
+            emin = min(emin, e);
+            emax = max(emax, e);
+          }
+        }
+        if (emin == INT_MAX) emin = emax = 0;
+        const bool wide = emax - emin > 20;
+        sm.emin[r] = emin;
+        sm.emax[r] = emax;
+        sm.wide[r] = wide;
+        sm.diag[r] = exact_dot(x, x, emin, emin, wide);
+      }
+      __syncwarp();
+      meta_ok = true;
+    };
+    // the float64 cosine of the reference arithmetic
+    auto cos64 = [&](int i, int j) -> double {
+      const double gii = sm.diag[i], gjj = sm.diag[j];
+      if (gii == 0.0 || gjj == 0.0) return 0.0;
+      const double g = exact_dot(row(i), row(j), sm.emin[i], sm.emin[j], sm.wide[i] | sm.wide[j]);
+      return __ddiv_rn(g, __dsqrt_rn(__dmul_rn(gii, gjj)));
+    };
+
+    // ---- Algorithm 1
     const int i0 = lane, i1 = lane + 32;
-    const bool live0 = i0 < n, live1 = i1 < n;
-    float a0 = 0.f, a1 = 0.f;
-    if (live0) {
-      float acc = 0.f;
-      for (int j = 0; j < n; ++j) acc = __fadd_rn(acc, sm.C(i0, j));
-      a0 = __fdiv_rn(acc, (float)n);
-    }
-    if (live1) {
-      float acc = 0.f;
-      for (int j = 0; j < n; ++j) acc = __fadd_rn(acc, sm.C(i1, j));
-      a1 = __fdiv_rn(acc, (float)n);
-    }
+    const bool live0 = i0 < n, live1 = NH > 1 && i1 < n;
     // exact mean cosine of candidate i: lanes evaluate cos64(i, j) for their j,
-    // lane 0 sums them left to right
+    // every lane sums them left to right
     auto mean64 = [&](int i) -> double {
-      for (int j = lane; j < n; j += 32) sm.v64[j] = cos64(sm, i, j);
+      meta();
+      for (int j = lane; j < n; j += 32) sm.v64[j] = cos64(i, j);
       __syncwarp();
       double acc = 0.0;
       for (int j = 0; j < n; ++j) acc = __dadd_rn(acc, sm.v64[j]);
       __syncwarp();
       return __ddiv_rn(acc, (double)n);
     };
-    const int p0 = filtered_argmin(sm, a0, a1, live0, live1, kMeanErr, mean64);
+    const int p0 = filtered_argmin(sm.cand, a[0], NH > 1 ? a[NH - 1] : 0.f, live0, live1, kMeanErr, mean64);
     if (lane == 0) sm.picks[0] = p0;
     bool ch0 = i0 == p0, ch1 = i1 == p0;
     float S0 = live0 ? sm.C(i0, p0) : 0.f, S1 = live1 ? sm.C(i1, p0) : 0.f;
     for (int k = 1; k < m; ++k) {
       // exact running maximum of candidate j over the picks so far
       auto smax64 = [&](int j) -> double {
+        meta();
         double v = -__longlong_as_double(0x7ff0000000000000LL);
         for (int q = lane; q < k; q += 32) {
-          const double c = cos64(sm, j, sm.picks[q]);
+          const double c = cos64(j, sm.picks[q]);
           v = c > v ? c : v;
         }
         return warp_max64(v);
       };
       __syncwarp();
-      const int r = filtered_argmin(sm, S0, S1, live0 && !ch0, live1 && !ch1, kCosErr, smax64);
+      const int r = filtered_argmin(sm.cand, S0, S1, live0 && !ch0, live1 && !ch1, kCosErr, smax64);
       if (i0 == r) ch0 = true;
       if (i1 == r) ch1 = true;
       if (live0) S0 = fmaxf(S0, sm.C(i0, r));
@@ -431,31 +443,59 @@ __global__ void __launch_bounds__(kThreads) fps_kernel(FpsParams P) {
     }
     __syncwarp();
     for (int k = lane; k < m; k += 32) trace[k] = (int8_t)sm.picks[k];
-    const unsigned m0 = __ballot_sync(0xFFFFFFFFu, ch0), m1 = __ballot_sync(0xFFFFFFFFu, ch1);
+    const unsigned m0 = __ballot_sync(kFull, ch0), m1 = __ballot_sync(kFull, ch1);
     const unsigned lt = (1u << lane) - 1u;
     if (ch0) sm.keep_src[__popc(m0 & lt)] = i0;
     if (ch1) sm.keep_src[__popc(m0) + __popc(m1 & lt)] = i1;
+  } else {
+    // nothing to sample: every candidate is kept in order
+    for (int k = lane; k < m; k += 32) trace[k] = k < n ? (int8_t)k : (int8_t)-1;
+    if (lane < n) sm.keep_src[lane] = lane;
   }
-  __syncthreads();
+  __syncwarp();
 
-  for (int idx = tid; idx < m * 16; idx += kThreads) bq[idx] = sm.x[sm.keep_src[idx >> 4] * 16 + (idx & 15)];
+  // ---- kept rows back into the beacon buffer; every source row is read
+  // before any is overwritten (m <= 31 rows of 16 uint4: <= 16 per lane)
+  const int kept = n < m ? n : m;
+  uint4 buf[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int idx = lane + 32 * q;
+    if (idx < kept * 16) buf[q] = row(sm.keep_src[idx >> 4])[idx & 15];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int idx = lane + 32 * q;
+    if (idx < kept * 16) bq[idx] = buf[q];
+  }
+}
+
+template <int NH>
+cudaError_t launch_nh(const FpsParams& p, cudaStream_t s) {
+  const size_t smem = WarpSmem<NH>::kBytes * kHeadsPerCta;
+  static std::atomic<unsigned long long> configured{0};  // one bit per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (!(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(fps_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  const int64_t blocks = (p.heads_total + kHeadsPerCta - 1) / kHeadsPerCta;
+  fps_kernel<NH><<<(unsigned)blocks, 32 * kHeadsPerCta, smem, s>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fps(const FpsParams& p, cudaStream_t s) {
   const int n = p.nb + p.nr;
-  if (p.heads_total <= 0 || p.m == 0) return cudaSuccess;
-  if (n > kMaxCand || n <= 0) return n <= 0 ? cudaSuccess : cudaErrorInvalidValue;
-  const size_t smem = fps_smem_bytes(n);
-  static size_t configured = 48 * 1024;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(fps_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
-  fps_kernel<<<(unsigned)p.heads_total, kThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  if (p.heads_total <= 0 || p.m == 0 || n <= 0) return cudaSuccess;
+  if (n > kMaxCand || p.m > 31) return cudaErrorInvalidValue;
+  return n <= 32 ? launch_nh<1>(p, s) : launch_nh<2>(p, s);
 }
 
 }  // namespace bkv

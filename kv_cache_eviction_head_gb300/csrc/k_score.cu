@@ -542,23 +542,29 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      long long g = 0;
+      long long g = 0;     // tiles issued
+      int st = 0;          // stage of tile g (g mod S)
+      uint32_t kph = 0;    // parity of (g div S)
       bool ok = true;
       for (int it = 0; it < mine && ok; ++it) {
         int layer, seq, kvh;
         unit_geom(blockIdx.x + it * gridDim.x, P.batch, P.kv_heads, layer, seq, kvh);
         const int row0 = (seq * P.kv_heads + kvh) * P.max_cache;
-        for (int s = 0; s < 2 * T; ++s, ++g) {
-          const int st = (int)(g % S);
-          if (g >= S && !mbar_wait(&kempty[st], (uint32_t)(((g / S) + 1) & 1), ctl, P.status)) {
+        for (int s = 0; s < 2 * T; ++s) {
+          if (g >= S && !mbar_wait(&kempty[st], kph ^ 1u, ctl, P.status)) {
             ok = false;
             break;
           }
-          const int kt = s % T;
+          const int kt = s < T ? s : s - T;
           mbar_expect_tx(&kfull[st], kTileBytes);
           const uint32_t dst = smem_u32(kst + (size_t)st * kTileBytes);
           tma_load_2d(dst, &P.kmap[layer], 0, row0 + kt * kTileKeys, &kfull[st]);
           tma_load_2d(dst + kSlabBytes, &P.kmap[layer], 64, row0 + kt * kTileKeys, &kfull[st]);
+          ++g;
+          if (++st == S) {
+            st = 0;
+            kph ^= 1u;
+          }
         }
       }
       // drain: every load issued has landed before the CTA may exit
@@ -572,7 +578,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      long long g = 0;
+      long long g = 0;   // tiles consumed
+      int st = 0;        // stage of tile g (g mod S)
+      uint32_t kph = 0;  // parity of (g div S)
       bool ok = true;
       const uint32_t qh = smem_u32(q_hi), ql = smem_u32(q_lo);
       const uint32_t slab_q = (uint32_t)lay.qrows * 128;  // bytes of one 64-column slab of the rows
@@ -580,8 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       for (int it = 0; it < mine && ok; ++it) {
         ok = mbar_wait(qready, (uint32_t)(it & 1), ctl, P.status);
         for (int s = 0; s < 2 * T && ok; ++s, ++g) {
-          const int st = (int)(g % S), b = (int)(g & 1);
-          ok = mbar_wait(&kfull[st], (uint32_t)((g / S) & 1), ctl, P.status);
+          const int b = (int)(g & 1);
+          ok = mbar_wait(&kfull[st], kph, ctl, P.status);
           if (ok && g >= 2) ok = mbar_wait(&tempty[b], (uint32_t)(((g >> 1) + 1) & 1), ctl, P.status);
           if (!ok) break;
           tc_fence_after();
@@ -616,6 +624,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
           }
           umma_commit(&kempty[st]);
           umma_commit(&tfull[b]);
+          if (++st == S) {
+            st = 0;
+            kph ^= 1u;
+          }
         }
         if (ok) umma_commit(qfree);  // arrives when every MMA that read this unit's rows is done
       }
@@ -637,10 +649,14 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       // copies, in increasing address order. A chunk's store overlaps only
       // sources that were loaded before it (its own and earlier chunks'), and
       // every later load reads above every earlier store's destination, so
-      // loads may run ahead of stores. One lane issues everything.
+      // loads may run ahead of stores. One lane issues everything; its buffer
+      // and phase counters wrap without division, since a 64-bit modulo per
+      // chunk costs more than the copy issue itself.
       if (lane == 0) {
-        long long cg = 0;  // global chunk counter: buffer cg % cbufs, phase (cg / cbufs) & 1
         const int CB = lay.cbufs, D = lay.D;
+        int4* cdesc = reinterpret_cast<int4*>(smem + lay.misc + 1536);  // [cbufs] tensor, source row, rows, shift
+        int lb = 0, sb = 0;  // next buffer to load into / to store from (loads and stores cycle alike)
+        uint32_t sph = 0;    // parity of buffer sb's next completion
         bool ok = true;
         for (int it = 0; it < mine && ok; ++it) {
           const int b = it & 1;
@@ -652,77 +668,71 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
           const size_t rowbase = (size_t)(seq * P.kv_heads + kvh) * P.max_cache;
           char* tb[2] = {reinterpret_cast<char*>(P.Kc[layer] + rowbase * kD),
                          reinterpret_cast<char*>(P.Vc[layer] + rowbase * kD)};
-          // chunk cursor: tensor t, run r, next source row
-          struct Cur {
-            int t, r, row;
-          };
-          auto start = [&](Cur& c) {
-            c.t = 0;
-            c.r = 0;
-            c.row = D > 0 ? dl[0] + 1 : L;
-          };
-          auto next = [&](Cur& c, int& t, int& src, int& n) -> bool {
-            while (c.t < 2 && D > 0) {
-              const int end = c.r + 1 < D ? dl[c.r + 1] : L;
-              if (c.row < end) {
-                n = end - c.row < kChunkRows ? end - c.row : kChunkRows;
-                t = c.t;
-                src = c.row;
-                c.row += n;
+          const int first = D > 0 ? dl[0] + 1 : L;  // lowest source row that moves
+          // chunk cursor over the runs of K, then of V: tensor ct, run cr, next source row crow
+          int ct = 0, cr = 0, crow = first;
+          auto next = [&](int4& c) -> bool {
+            while (ct < 2 && D > 0) {
+              const int end = cr + 1 < D ? dl[cr + 1] : L;
+              if (crow < end) {
+                const int n = end - crow < kChunkRows ? end - crow : kChunkRows;
+                c = make_int4(ct, crow, n, cr + 1);  // run cr moves down by cr + 1 slots
+                crow += n;
                 return true;
               }
-              if (++c.r < D) {
-                c.row = dl[c.r] + 1;
+              if (++cr < D) {
+                crow = dl[cr] + 1;
               } else {
-                ++c.t;
-                c.r = 0;
-                c.row = dl[0] + 1;
+                ++ct;
+                cr = 0;
+                crow = first;
               }
             }
             return false;
           };
-          Cur lc, sc2;
-          start(lc);
-          start(sc2);
+          auto load = [&](const int4& c) {
+            cdesc[lb] = c;
+            const uint32_t bytes = (uint32_t)c.z * (kD * 2);
+            mbar_expect_tx(&cfull[lb], bytes);
+            bulk_load(smem_u32(cst + (size_t)lb * kChunkBytes), tb[c.x] + (size_t)c.y * (kD * 2), bytes, &cfull[lb]);
+            lb = lb + 1 == CB ? 0 : lb + 1;
+          };
           bulk_wait_read<0>();  // the previous unit's stores are done reading every chunk buffer
-          long long nl = 0, ns = 0;
-          int t, src, n;
-          while (nl < CB - 1 && next(lc, t, src, n)) {
-            const long long gi = cg + nl;
-            uint64_t* bar = &cfull[gi % CB];
-            mbar_expect_tx(bar, (uint32_t)(n * kD * 2));
-            bulk_load(smem_u32(cst + (gi % CB) * kChunkBytes), tb[t] + (size_t)src * kD * 2, (uint32_t)(n * kD * 2), bar);
-            ++nl;
+          int inflight = 0;
+          int4 c;
+          while (inflight < CB - 1 && next(c)) {
+            load(c);
+            ++inflight;
           }
-          while (ns < nl && ok) {
-            int st2, ssrc, sn;
-            next(sc2, st2, ssrc, sn);
-            const long long gi = cg + ns;
-            ok = mbar_wait(&cfull[gi % CB], (uint32_t)((gi / CB) & 1), ctl, P.status);
+          while (inflight > 0) {
+            ok = mbar_wait(&cfull[sb], sph, ctl, P.status);
             if (!ok) break;
-            const int shift = sc2.r + 1;  // run index of the chunk just taken, plus one
-            bulk_store(tb[st2] + (size_t)(ssrc - shift) * kD * 2, smem_u32(cst + (gi % CB) * kChunkBytes),
-                       (uint32_t)(sn * kD * 2));
+            const int4 d = cdesc[sb];
+            bulk_store(tb[d.x] + (size_t)(d.y - d.w) * (kD * 2), smem_u32(cst + (size_t)sb * kChunkBytes),
+                       (uint32_t)d.z * (kD * 2));
             bulk_commit();
-            ++ns;
-            if (next(lc, t, src, n)) {
-              bulk_wait_read<1>();  // the buffer of chunk ns - 2 (reused now) has been read out
-              const long long gl = cg + nl;
-              uint64_t* bar = &cfull[gl % CB];
-              mbar_expect_tx(bar, (uint32_t)(n * kD * 2));
-              bulk_load(smem_u32(cst + (gl % CB) * kChunkBytes), tb[t] + (size_t)src * kD * 2,
-                        (uint32_t)(n * kD * 2), bar);
-              ++nl;
+            if (++sb == CB) {
+              sb = 0;
+              sph ^= 1u;
+            }
+            --inflight;
+            if (next(c)) {
+              bulk_wait_read<1>();  // the buffer reused now belonged to the store before the last one
+              load(c);
+              ++inflight;
             }
           }
           if (!ok) {  // after an abort, loads already issued must land before the CTA exits
-            for (long long gi = cg + ns; gi < cg + nl; ++gi) {
+            for (; inflight > 0; --inflight) {
               const long long t0 = clock64();
-              while (!mbar_test(&cfull[gi % CB], (uint32_t)((gi / CB) & 1)) && clock64() - t0 < kWaitCycles) {
+              while (!mbar_test(&cfull[sb], sph) && clock64() - t0 < kWaitCycles) {
+              }
+              if (++sb == CB) {
+                sb = 0;
+                sph ^= 1u;
               }
             }
           }
-          cg += nl;
           if (ok && D > 0 && P.rows_moved)
             atomicAdd(P.rows_moved, (unsigned long long)(L - D - dl[0]));
           mbar_arrive(&dfree[b]);
