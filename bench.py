@@ -461,7 +461,7 @@ def main():
     ap.add_argument("--workload", default="qwen3_4b_b192")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller cases for profiling)")
-    ap.add_argument("--cpu-units", type=int, default=192)
+    ap.add_argument("--cpu-units", type=int, default=1024)
     ap.add_argument("--ref-units-per-step", type=int, default=32)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

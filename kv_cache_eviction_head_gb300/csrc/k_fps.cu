@@ -226,7 +226,7 @@ __device__ __forceinline__ float unkey(uint32_t k) {
 // for close candidates come from exact(j), evaluated cooperatively by the
 // warp (same value on every lane). Returns the winning index on every lane.
 template <class Exact>
-__device__ int filtered_argmin(int* cand, float v0, float v1, bool ok0, bool ok1, float err, Exact exact) {
+__device__ __forceinline__ int filtered_argmin(int* cand, float v0, float v1, bool ok0, bool ok1, float err, Exact exact) {
   const int lane = threadIdx.x & 31;
   const uint32_t k = min(ok0 ? fkey(v0) : 0xFFFFFFFFu, ok1 ? fkey(v1) : 0xFFFFFFFFu);
   const float m = unkey(__reduce_min_sync(kFull, k));
@@ -258,7 +258,7 @@ __device__ int filtered_argmin(int* cand, float v0, float v1, bool ok0, bool ok1
 }
 
 template <int NH>
-__global__ void __launch_bounds__(32 * kHeadsPerCta) fps_kernel(FpsParams P) {
+__global__ void __launch_bounds__(32 * kHeadsPerCta, 6) fps_kernel(FpsParams P) {
   using W = WarpSmem<NH>;
   constexpr int NT = W::NT;
   extern __shared__ __align__(16) unsigned char fps_smem[];
@@ -277,29 +277,41 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta) fps_kernel(FpsParams P) {
 
   if (n > m) {
     // ---- rows -> float32, each scaled so its largest component lies in [1, 4)
-    // lanes 0-15 take one row, lanes 16-31 the next; padding rows are zero
+    // lanes 0-15 take one row, lanes 16-31 the next; padding rows are zero.
+    // A batch of rows is loaded before any is processed (one memory latency
+    // per batch instead of one per row pair).
+    constexpr int kLoadBatch = 8;
     bool bad = false;
-    for (int r0 = 0; r0 < NT; r0 += 2) {
-      const int r = r0 + (lane >> 4), part = lane & 15;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < n) v = __ldg(row(r) + part);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t e = 0;
+    const int part = lane & 15;
+#pragma unroll 1
+    for (int r0 = 0; r0 < NT; r0 += 2 * kLoadBatch) {
+      uint4 vb[kLoadBatch];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) e = max(e, max((w[q] >> 7) & 0xFFu, (w[q] >> 23) & 0xFFu));
-#pragma unroll
-      for (int off = 1; off < 16; off <<= 1) e = max(e, __shfl_xor_sync(kFull, e, off));
-      bad |= e == 0xFFu;
-      const float scale = __int_as_float(max(254 - (int)e, 1) << 23);  // 2^(127 - e)
-      float f[8];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        f[2 * q] = __fmul_rn(__uint_as_float(w[q] << 16), scale);
-        f[2 * q + 1] = __fmul_rn(__uint_as_float(w[q] & 0xFFFF0000u), scale);
+      for (int bi = 0; bi < kLoadBatch; ++bi) {
+        const int r = r0 + 2 * bi + (lane >> 4);
+        vb[bi] = r < n ? __ldg(row(r) + part) : make_uint4(0, 0, 0, 0);
       }
-      float4* dst = reinterpret_cast<float4*>(sm.y + r * kYStride + part * 8);
-      dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-      dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+#pragma unroll
+      for (int bi = 0; bi < kLoadBatch; ++bi) {
+        const int r = r0 + 2 * bi + (lane >> 4);
+        const uint32_t w[4] = {vb[bi].x, vb[bi].y, vb[bi].z, vb[bi].w};
+        uint32_t e = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) e = max(e, max((w[q] >> 7) & 0xFFu, (w[q] >> 23) & 0xFFu));
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1) e = max(e, __shfl_xor_sync(kFull, e, off));
+        bad |= e == 0xFFu;
+        const float scale = __int_as_float(max(254 - (int)e, 1) << 23);  // 2^(127 - e)
+        float f[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          f[2 * q] = __fmul_rn(__uint_as_float(w[q] << 16), scale);
+          f[2 * q + 1] = __fmul_rn(__uint_as_float(w[q] & 0xFFFF0000u), scale);
+        }
+        float4* dst = reinterpret_cast<float4*>(sm.y + r * kYStride + part * 8);
+        dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+        dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+      }
     }
     if (__any_sync(kFull, bad) && lane == 0) latch(P.status, BKV_ERR_NONFINITE);
     __syncwarp();

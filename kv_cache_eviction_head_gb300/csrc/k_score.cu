@@ -108,24 +108,51 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Ctl* ctl
   return true;
 }
 
+// ------------------------------------------------------------------ L2 policies
+// K tiles are read twice (pass 1, then pass 2 once every row's log-sum-exp is
+// known); the compaction streams rows it touches once. Pass-1 loads keep their
+// lines (evict_last) so that pass 2 finds them in L2, and pass 2 walks the
+// tiles in reverse, newest first: when a unit's tiles do not all stay in L2,
+// the ones pass 1 read last are the ones still there. Every compaction copy
+// marks its lines evict_first.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
+                                            uint64_t* bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 
 // Non-tensor bulk copies: global -> shared with an mbarrier, shared -> global
 // in bulk groups.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(dst), "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
 }
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+               ::"l"(dst), "r"(src), "r"(bytes), "l"(policy)
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -546,6 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       int st = 0;          // stage of tile g (g mod S)
       uint32_t kph = 0;    // parity of (g div S)
       bool ok = true;
+      const uint64_t keep = policy_evict_last(), stream = policy_evict_normal();
       for (int it = 0; it < mine && ok; ++it) {
         int layer, seq, kvh;
         unit_geom(blockIdx.x + it * gridDim.x, P.batch, P.kv_heads, layer, seq, kvh);
@@ -555,11 +583,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
             ok = false;
             break;
           }
-          const int kt = s < T ? s : s - T;
+          const int kt = s < T ? s : 2 * T - 1 - s;  // pass 2 walks the tiles backwards
           mbar_expect_tx(&kfull[st], kTileBytes);
           const uint32_t dst = smem_u32(kst + (size_t)st * kTileBytes);
-          tma_load_2d(dst, &P.kmap[layer], 0, row0 + kt * kTileKeys, &kfull[st]);
-          tma_load_2d(dst + kSlabBytes, &P.kmap[layer], 64, row0 + kt * kTileKeys, &kfull[st]);
+          const uint64_t pol = s < T ? keep : stream;
+          tma_load_2d(dst, &P.kmap[layer], 0, row0 + kt * kTileKeys, &kfull[st], pol);
+          tma_load_2d(dst + kSlabBytes, &P.kmap[layer], 64, row0 + kt * kTileKeys, &kfull[st], pol);
           ++g;
           if (++st == S) {
             st = 0;
@@ -658,6 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
         int lb = 0, sb = 0;  // next buffer to load into / to store from (loads and stores cycle alike)
         uint32_t sph = 0;    // parity of buffer sb's next completion
         bool ok = true;
+        const uint64_t stream = policy_evict_first();
         for (int it = 0; it < mine && ok; ++it) {
           const int b = it & 1;
           ok = mbar_wait(&dready[b], (uint32_t)((it >> 1) & 1), ctl, P.status);
@@ -694,7 +724,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
             cdesc[lb] = c;
             const uint32_t bytes = (uint32_t)c.z * (kD * 2);
             mbar_expect_tx(&cfull[lb], bytes);
-            bulk_load(smem_u32(cst + (size_t)lb * kChunkBytes), tb[c.x] + (size_t)c.y * (kD * 2), bytes, &cfull[lb]);
+            bulk_load(smem_u32(cst + (size_t)lb * kChunkBytes), tb[c.x] + (size_t)c.y * (kD * 2), bytes, &cfull[lb],
+                      stream);
             lb = lb + 1 == CB ? 0 : lb + 1;
           };
           bulk_wait_read<0>();  // the previous unit's stores are done reading every chunk buffer
@@ -709,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
             if (!ok) break;
             const int4 d = cdesc[sb];
             bulk_store(tb[d.x] + (size_t)(d.y - d.w) * (kD * 2), smem_u32(cst + (size_t)sb * kChunkBytes),
-                       (uint32_t)d.z * (kD * 2));
+                       (uint32_t)d.z * (kD * 2), stream);
             bulk_commit();
             if (++sb == CB) {
               sb = 0;
@@ -803,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
           if (!ok) break;
           tc_fence_after();
           const uint32_t col0 = tmem + lane_base + (uint32_t)(b * lay.bufcols);
-          const int kt = s % T;
+          const int kt = s < T ? s : 2 * T - 1 - s;
           if (s < T) {
             // pass 1: this thread owns observation row et (and a row of the second M tile)
             for (int mt = 0; mt < lay.mtiles; ++mt) {
