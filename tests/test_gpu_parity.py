@@ -85,6 +85,30 @@ def test_qwen3_4b_b192_full_size_sampled_units():
     assert rep.units_checked == len(units) * rep.evictions
 
 
+def test_qwen3_14b_b64_full_size_sampled_units():
+    """Qwen3-14B head shape (GQA 5, 160 observation rows, budget 1024) at
+    batch 64: full-size cache, three evictions, sampled units."""
+    w = WORKLOADS["qwen3_14b_b64"]
+    units = [(0, 0, 0), (39, 63, 7), (20, 31, 4), (7, 50, 1), (33, 12, 6), (39, 0, 3)]
+    rep = run_lockstep(w, seed=0xBEAC3, sample_units=units, gen_device="cuda",
+                       steps=w.max_cache + 2 * w.period)
+    assert_clean(rep, min_evictions=3)
+    assert rep.units_checked == len(units) * rep.evictions
+
+
+@pytest.mark.parametrize("budget", [256, 1024, 4096])
+def test_r1_qwen7b_b128_full_size_sampled_units(budget):
+    """R1-Distill-Qwen-7B head shape (GQA 7, 224 observation rows, theta 1e4)
+    at batch 128 over the budget sweep's small, middle and largest budgets:
+    full-size cache, three evictions, sampled units."""
+    w = WORKLOADS[f"r1_qwen7b_b128_k{budget}"]
+    units = [(0, 0, 0), (27, 127, 3), (13, 64, 1), (5, 100, 2), (21, 7, 0)]
+    rep = run_lockstep(w, seed=0xBEAC4 + budget, sample_units=units, gen_device="cuda",
+                       steps=w.max_cache + 2 * w.period)
+    assert_clean(rep, min_evictions=3)
+    assert rep.units_checked == len(units) * rep.evictions
+
+
 def wide_queries(t, q):
     """Replaces some queries by vectors whose exponents span far more than 20
     binades (FPS's wide exact-sum path), by zero rows and by exact duplicates."""
