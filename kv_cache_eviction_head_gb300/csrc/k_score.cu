@@ -156,6 +156,9 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t byt
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
@@ -326,6 +329,8 @@ __device__ void select_keep(const float* sc, int L, int prefix, int recent, int 
 
 constexpr int kChunkRows = 32;                   // rows per compaction chunk
 constexpr int kChunkBytes = kChunkRows * kD * 2;  // 8 KB
+constexpr int kPfRows = 512;                      // L2 prefetch lead of the copier (few chunk buffers only)
+constexpr int kPfPieceRows = 64;                  // rows per L2 prefetch
 
 struct Layout {
   int R, Rp16, mtiles, qrows, rows64;  // rows, rows to 16, M tiles, rows allocated, rows to 64
@@ -720,6 +725,24 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
             }
             return false;
           };
+          // With few chunk buffers the loads alone keep too few bytes in
+          // flight to cover HBM latency; the moved rows [first, L) of K, then
+          // of V, are then prefetched into L2 kPfRows rows ahead of them.
+          const bool pf_on = CB <= 4;
+          const int moved = L - first;
+          int pf_row = 0;  // rows prefetched so far, K's moved rows then V's
+          auto prefetch_to = [&](int target) {
+            target = target < 2 * moved ? target : 2 * moved;
+            while (pf_row < target) {
+              const int pt = pf_row >= moved ? 1 : 0;
+              const int off = pf_row - (pt ? moved : 0);
+              int nr = moved - off < kPfPieceRows ? moved - off : kPfPieceRows;
+              nr = target - pf_row < nr ? target - pf_row : nr;
+              bulk_prefetch_l2(tb[pt] + (size_t)(first + off) * (kD * 2), (uint32_t)nr * (kD * 2));
+              pf_row += nr;
+            }
+          };
+          if (pf_on) prefetch_to(kPfRows);
           auto load = [&](const int4& c) {
             cdesc[lb] = c;
             const uint32_t bytes = (uint32_t)c.z * (kD * 2);
@@ -727,6 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
             bulk_load(smem_u32(cst + (size_t)lb * kChunkBytes), tb[c.x] + (size_t)c.y * (kD * 2), bytes, &cfull[lb],
                       stream);
             lb = lb + 1 == CB ? 0 : lb + 1;
+            if (pf_on) prefetch_to((c.x ? moved : 0) + c.y + c.z - first + kPfRows);
           };
           bulk_wait_read<0>();  // the previous unit's stores are done reading every chunk buffer
           int inflight = 0;
