@@ -30,7 +30,9 @@
 //              pass 2  D[key][row] = K_tile . Q^T   (M = 128 keys, N = rows)
 //            so each epilogue thread owns one TMEM lane (a row in pass 1, a
 //            key in pass 2) and reduces along its own registers only;
-//   warp 2   warms L2 with the next unit's source rows;
+//   warp 2   compacts K and V of a unit whose keep set is known, with bulk
+//            copies through shared memory, while later units are scored
+//            (without compaction: warms L2 with the next unit's rows);
 //   warp 3   selects the keep set of a finished unit from its scores;
 //   warps 4-11  epilogue, two warpgroups taking alternate TMEM buffers:
 //            TMEM -> registers, online log-sum-exp in pass 1, max-pooling in
@@ -42,9 +44,10 @@
 //
 // Selection drops the D = L - budget lowest-scoring candidates among slots
 // [prefix, L - recent); among equal scores the higher slot is dropped first,
-// so the lower slot wins a tie. A 4 x 8-bit radix select over the fp32 score
-// bits (scores are >= 0, so the bit patterns order like the values) finds the
-// D-th smallest score, then a scan places the kept slots in order.
+// so the lower slot wins a tie. Scores are >= 0, so their fp32 bit patterns
+// order like the values: each lane keeps a sorted list of its smallest
+// (score bits, ~slot) keys, the warp extracts the D smallest from the list
+// heads, and a ballot scan writes the kept (and dropped) slots in order.
 #include "bkv_internal.cuh"
 
 namespace bkv {
