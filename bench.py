@@ -181,6 +181,37 @@ def oracle_rate(w, n_units: int, pool, cores: int, seed: int = 1234):
             "cpu_s": sum(times), "units": n_units}
 
 
+def single_thread_rate(w, n_units: int, seed: int = 4321):
+    """Evictions/s of the CPU oracle on one core (a one-process pool, one BLAS thread)."""
+    import multiprocessing as mp
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+    with mp.get_context("spawn").Pool(1) as pool:
+        r = oracle_rate(w, n_units, pool, 1, seed=seed)
+    # the per-unit eviction times alone (the worker's start-up and imports excluded)
+    r["value"] = n_units / r["cpu_s"] / w.kv_heads
+    return r
+
+
+def cpu_model() -> str:
+    """The host CPU's model name, from /proc/cpuinfo (x86 'model name', Arm implementer/part)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read().splitlines()
+    except OSError:
+        return "unknown"
+    fields = {}
+    for line in info:
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU implementer" in fields:
+        return f"Arm implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    return "unknown"
+
+
 def run_reference(args, w):
     rank, _, world = dist_env()
     if rank != 0:
@@ -288,14 +319,15 @@ def run_ours(args, w):
         dist.barrier()
     torch.cuda.synchronize(dev)
     sampler.start()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(cs)
-    for _ in range(args.steps):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(cs)
+    for i in range(args.steps):
         step()
-    e1.record(cs)
+        evs[i + 1].record(cs)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
-    elapsed_ms = e0.elapsed_time(e1)
+    elapsed_ms = evs[0].elapsed_time(evs[-1])
+    step_ms = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
     ktimes = bkv.bkv_profile_read(h)
     bkv.bkv_profile(h, False)
     bkv.bkv_sync(h)
@@ -350,10 +382,14 @@ def run_ours(args, w):
         pool, cores = oracle_pool()
         with pool:
             r = oracle_rate(w, args.cpu_units, pool, cores)
+        single = single_thread_rate(w, max(8, args.cpu_units // 32))
         cpu = {"value": r["value"], "unit": "evictions/s", "cores": r["cores"], "kind": "oracle",
                "sample": f"{r['units']} steady-state units of {w.name} (one eviction = "
                          f"{w.kv_heads} units), fp64 oracle, one unit per process, "
-                         f"{r['cpu_s']:.1f} s of CPU work in {r['wall_s']:.1f} s"}
+                         f"{r['cpu_s']:.1f} s of CPU work in {r['wall_s']:.1f} s",
+               "single_thread": {"value": single["value"], "unit": "evictions/s",
+                                 "units": single["units"]},
+               "cpu_model": cpu_model()}
 
     if rank == 0:
         out = {
@@ -362,6 +398,8 @@ def run_ours(args, w):
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "us_per_eviction": 1e3 * elapsed_ms / args.steps / evictions_per_step,
+            "step_ms": {"median": statistics.median(step_ms),
+                        "p95": step_ms[min(len(step_ms) - 1, math.ceil(0.95 * len(step_ms)) - 1)]},
             "config": {"workload": w.name, "layers": w.layers, "batch": w.batch,
                        "heads": w.heads, "kv_heads": w.kv_heads, "d": w.d, "budget": w.budget,
                        "period": w.period, "prefix": w.prefix, "recent": w.recent,
