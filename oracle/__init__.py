@@ -25,10 +25,11 @@ from .beaconkv import (
     attention_weights,
     max_pool,
     select_keep,
+    order_free_layout,
     UnitOracle,
 )
 
 __all__ = [
     "bf16_to_f64", "rope", "exact_dot", "gram_exact", "cosine_matrix", "fps",
-    "attention_weights", "max_pool", "select_keep", "UnitOracle",
+    "attention_weights", "max_pool", "select_keep", "order_free_layout", "UnitOracle",
 ]

@@ -199,6 +199,27 @@ def select_keep(score, L: int, prefix: int, recent: int, budget: int) -> list[in
     return sorted(keep | set(order[:k_sel]))
 
 
+def order_free_layout(kept, budget: int) -> list[int]:
+    """Slot layout of an order-free compaction, a relaxation of eq. 8's Sort.
+
+    The kept set is the one eq. 8 selects (`kept`, any order). Instead of
+    gathering it in slot order, every kept slot below `budget` stays where it
+    is and the dropped slots below `budget` (the holes, ascending) receive the
+    kept slots at or above `budget` (ascending). Returns `layout`: after the
+    compaction slot i holds the row that was in slot layout[i]. Exactly as many
+    rows move as there are holes.
+    """
+    ks = sorted(int(j) for j in kept)
+    inside = set(j for j in ks if j < budget)
+    holes = [i for i in range(budget) if i not in inside]
+    tail = [j for j in ks if j >= budget]
+    assert len(holes) == len(tail), "a keep set of `budget` slots has one tail slot per hole"
+    layout = list(range(budget))
+    for i, j in zip(holes, tail):
+        layout[i] = j
+    return layout
+
+
 # ----------------------------------------------------------------------------
 # the per-unit state machine (BeaconKV reading notes, §2.2 eq. 9 and Algorithm 2)
 
@@ -213,10 +234,11 @@ class HeadState:
 
 @dataclass
 class EvictResult:
-    kept: list
+    kept: list          # the keep set this oracle selected, ascending
     score: np.ndarray
     obs_rows: int
     traces: list
+    layout: list = field(default_factory=list)   # source slot of each slot after compaction
 
 
 class UnitOracle:
@@ -231,10 +253,14 @@ class UnitOracle:
       evict(t):     observation rows RoPE(Bq, t) and RoPE(q, tau) for <q, tau>
                     in R, per head; score, keep, compact; then per head
                     Bq <- FPS(Bq + R, fps_keep) and R <- empty (Algorithm 2).
+    With order_free, the compaction keeps the same set but in the layout of
+    order_free_layout (holes below the budget filled from the tail); keys
+    carry their positions, so later masking is unchanged.
     """
 
     def __init__(self, group: int, d: int, theta: float, budget: int, prefix: int,
-                 recent: int, fps_cap: int, fps_keep: int):
+                 recent: int, fps_cap: int, fps_keep: int, order_free: bool = False):
+        self.order_free = order_free
         self.group, self.d, self.theta = group, d, theta
         self.budget, self.prefix, self.recent = budget, prefix, recent
         self.fps_cap, self.fps_keep = fps_cap, fps_keep
@@ -294,10 +320,11 @@ class UnitOracle:
         else:
             nobs = self.observation(t)[0].shape[0]
         kept = select_keep(score, L, self.prefix, self.recent, self.budget)
-        use = list(kept_override) if kept_override is not None else kept
-        self.K = [self.K[i] for i in use]
-        self.V = [self.V[i] for i in use]
-        self.pos = [self.pos[i] for i in use]
+        use = sorted(kept_override) if kept_override is not None else kept
+        layout = order_free_layout(use, self.budget) if self.order_free else use
+        self.K = [self.K[i] for i in layout]
+        self.V = [self.V[i] for i in layout]
+        self.pos = [self.pos[i] for i in layout]
         traces = []
         for st in self.heads:
             X = st.bq + [q for q, _ in st.rq]
@@ -309,7 +336,7 @@ class UnitOracle:
                 st.bq = X
             st.rq.clear()
             traces.append(list(st.trace))
-        return EvictResult(kept=kept, score=score, obs_rows=nobs, traces=traces)
+        return EvictResult(kept=kept, score=score, obs_rows=nobs, traces=traces, layout=layout)
 
     # -- state injection (steady-state samples for timing) -------------------
     def load_state(self, bq_rows, rq_rows, rq_pos, K, V, pos) -> None:

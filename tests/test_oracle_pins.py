@@ -18,7 +18,7 @@ import pytest
 import torch
 
 from oracle import (UnitOracle, attention_weights, bf16_to_f64, cosine_matrix, exact_dot, fps,
-                    gram_exact, max_pool, rope, select_keep)
+                    gram_exact, max_pool, order_free_layout, rope, select_keep)
 from synth import kv_bytes_per_token, to_bits
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -345,6 +345,68 @@ def test_compaction_is_a_bytewise_gather():
     assert np.array_equal(np.stack(u.K), rows[res.kept])
     assert np.array_equal(np.stack(u.V), vals[res.kept])
     assert u.pos == res.kept
+
+
+def test_order_free_layout_golden():
+    gd = read_golden("order_free_layout.txt")
+    score = np.array([float(x) for x in gd["scores"].split(",")])
+    L, budget, prefix, recent = (int(gd[k]) for k in ("L", "budget", "prefix", "recent"))
+    kept = select_keep(score, L, prefix, recent, budget)
+    assert kept == [int(x) for x in gd["kept"].split(",")]
+    layout = order_free_layout(kept, budget)
+    assert layout == [int(x) for x in gd["layout"].split(",")]
+    assert sum(1 for i, j in enumerate(layout) if i != j) == int(gd["moved"])
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_order_free_layout_properties(seed):
+    """Against the definition restated slot by slot: kept slots below the budget
+    stay, holes take the tail in order, and the layout is the keep set."""
+    g = np.random.default_rng(seed)
+    L = int(g.integers(20, 400))
+    budget = int(g.integers(1, L))
+    kept = sorted(g.choice(L, size=budget, replace=False).tolist())
+    layout = order_free_layout(kept, budget)
+    assert sorted(layout) == kept
+    tail = iter(j for j in kept if j >= budget)
+    moved = 0
+    for i in range(budget):
+        if i in kept:
+            assert layout[i] == i
+        else:
+            assert layout[i] == next(tail)
+            moved += 1
+    assert moved == sum(1 for j in kept if j >= budget) <= L - budget
+
+
+@pytest.mark.parametrize("recent,period", [(4, 6), (6, 6), (0, 5)])
+def test_order_free_stream_keeps_the_same_tokens(recent, period):
+    """With the recent window inside the appended tail (recent <= period), an
+    order-free stream keeps exactly the tokens (by position), the K/V rows and
+    the FPS picks of the sorted stream at every eviction; only the slot layout
+    differs. Slot-based prefix/recent protection and masking therefore keep
+    their positional meaning after holes are filled from the tail."""
+    budget, prefix = 24, 2
+    mk = lambda of: UnitOracle(group=2, d=128, theta=1e6, budget=budget, prefix=prefix,
+                               recent=recent, fps_cap=6, fps_keep=3, order_free=of)
+    a, b = mk(False), mk(True)
+    keys, vals = rand_bits((200, 128), seed=31), rand_bits((200, 128), seed=32)
+    qs = rand_bits((200, 2, 128), seed=33)
+    evictions = 0
+    for t in range(200):
+        for u in (a, b):
+            u.append_kv(keys[t], vals[t], t)
+            u.append_queries(qs[t], t)
+        if len(a.K) == budget + period:
+            ra, rb = a.evict(t), b.evict(t)
+            evictions += 1
+            assert ra.traces == rb.traces
+            assert sorted(a.pos) == sorted(b.pos)
+            by_pos = {p: (k.tobytes(), v.tobytes()) for p, k, v in zip(b.pos, b.K, b.V)}
+            assert all(by_pos[p] == (k.tobytes(), v.tobytes()) for p, k, v in zip(a.pos, a.K, a.V))
+            assert a.pos == sorted(a.pos)
+            assert sum(1 for i, j in enumerate(rb.layout) if i != j) <= period
+    assert evictions >= 10
 
 
 # ---------------------------------------------------------------------------- state machine
