@@ -274,7 +274,8 @@ def run_ours(args, w):
     cfg = bkv.make_config(heads=w.heads, kv_heads=w.kv_heads, d=w.d, budget=w.budget,
                           period=w.period, prefix=w.prefix, recent=w.recent, fps_cap=w.fps_cap,
                           fps_keep=w.fps_keep, layers=w.layers, batch=w.batch,
-                          max_cache=w.max_cache, rope_theta=w.theta)
+                          max_cache=w.max_cache, rope_theta=w.theta,
+                          flags=bkv.BKV_FLAG_ORDER_FREE if args.order_free else 0)
     ws = torch.empty(bkv.bkv_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
     cs = torch.cuda.current_stream(dev)
     h = bkv.bkv_create(cfg, ws, cs)
@@ -406,7 +407,9 @@ def run_ours(args, w):
                        "fps": f"{w.fps_cap}->{w.fps_keep}", "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (K/V cache %.1f GB)" % (
                            2 * w.layers * w.batch * w.kv_heads * w.max_cache * w.d * 2 / 1e9),
-                       "step": f"1 eviction + {w.period} query appends"},
+                       "step": f"1 eviction + {w.period} query appends",
+                       "compaction": "order-free (holes filled from the kept tail)" if args.order_free
+                       else "slot order (eq. 8)"},
             "gpu_launches": int(sum(n for _, n in ktimes.values())),
             "roofline": roofline,
             "path": {"alg_bytes_per_step": pbytes,
@@ -501,6 +504,8 @@ def main():
                     help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--cpu-units", type=int, default=1024)
     ap.add_argument("--ref-units-per-step", type=int, default=32)
+    ap.add_argument("--order-free", action="store_true",
+                    help="order-free compaction (BKV_FLAG_ORDER_FREE) instead of slot order")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()

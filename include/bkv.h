@@ -60,6 +60,15 @@ typedef enum bkv_status {
 
 /* Keep each eviction's Score[j] in the workspace for bkv_get_scores. */
 #define BKV_FLAG_KEEP_SCORES 1
+/* Order-free compaction, a relaxation of eq. 8's Sort (notes §2.3): the same
+ * keep set, but kept slots below the budget stay where they are and the
+ * dropped slots below the budget (ascending) take the kept slots at or above
+ * the budget (ascending), so at most cache_len - budget rows move instead of
+ * every row after the first dropped slot. Slots [0, budget) then hold the
+ * kept tokens out of position order; the appended slots [budget, cache_len)
+ * stay in position order, which the next eviction's recent window and causal
+ * mask rely on, so bkv_evict requires recent <= cache_len - budget. */
+#define BKV_FLAG_ORDER_FREE 2
 
 typedef struct bkv_config {
   int32_t heads;      /* query heads per layer, H                                   */
@@ -131,11 +140,15 @@ bkv_status bkv_append_queries(bkv_handle h, const void* q_pre, int64_t step);
  *          budget < cache_len <= max_cache; BKV_ERR_STATE otherwise.
  *   step:  must equal the step of the last bkv_append_queries.
  *   kept:  device int32 [layers][batch][kv_heads][budget]; receives I_final,
- *          ascending slot indices into the pre-eviction cache.
- * On completion slots [0, budget) of every unit hold K[I_final] / V[I_final];
+ *          ascending slot indices into the pre-eviction cache. With
+ *          BKV_FLAG_ORDER_FREE it receives the layout instead: kept[i] is the
+ *          pre-eviction slot whose row now sits in slot i (the same set, not
+ *          ascending).
+ * On completion slots [0, budget) of every unit hold K[kept] / V[kept];
  * slots [budget, cache_len) are left with unspecified contents. Then every
  * query head's beacons become FPS(beacons + recents, fps_keep) and its recent
- * ring is emptied. BKV_ERR_UNSUPPORTED if G * (beacons + recents) > 256. */
+ * ring is emptied. BKV_ERR_UNSUPPORTED if G * (beacons + recents) > 256;
+ * BKV_ERR_INVALID_ARG with BKV_FLAG_ORDER_FREE if recent > cache_len - budget. */
 bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache_len,
                      int64_t step, int32_t* kept);
 

@@ -33,7 +33,7 @@ bkv_status check_config(const bkv_config* c) {
   if (c->fps_cap <= 0 || c->fps_keep < 0 || c->fps_keep >= c->fps_cap) return BKV_ERR_INVALID_ARG;
   if (c->layers <= 0 || c->batch <= 0 || c->max_cache <= c->budget) return BKV_ERR_INVALID_ARG;
   if (!(c->rope_theta > 0.0)) return BKV_ERR_INVALID_ARG;
-  if (c->flags & ~BKV_FLAG_KEEP_SCORES) return BKV_ERR_INVALID_ARG;
+  if (c->flags & ~(BKV_FLAG_KEEP_SCORES | BKV_FLAG_ORDER_FREE)) return BKV_ERR_INVALID_ARG;
   if (c->d != bkv::kD || c->fps_cap > bkv::kMaxFpsCap || c->layers > bkv::kMaxLayers)
     return BKV_ERR_UNSUPPORTED;
   const int64_t units = (int64_t)c->layers * c->batch * c->kv_heads;
@@ -247,9 +247,12 @@ bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache
   if (h->last_step < 0 || step != h->last_step) return BKV_ERR_STATE;
   if (cache_len != h->cache_len || cache_len <= c.budget || cache_len > c.max_cache)
     return BKV_ERR_STATE;
+  const bool order_free = (c.flags & BKV_FLAG_ORDER_FREE) != 0;
+  if (order_free && c.recent > cache_len - c.budget) return BKV_ERR_INVALID_ARG;
+  const int compact = order_free ? 2 : 1;
   const int R = h->group * (h->nb + h->nr);
   if (R > bkv::kMaxObsRows || cache_len > 8192) return BKV_ERR_UNSUPPORTED;
-  if (bkv::score_smem_bytes(R, cache_len, h->nr, c.budget, 1) > kMaxSmem) return BKV_ERR_UNSUPPORTED;
+  if (bkv::score_smem_bytes(R, cache_len, h->nr, c.budget, compact) > kMaxSmem) return BKV_ERR_UNSUPPORTED;
 
   const int ring_first = h->ring_slot(step - h->nr + 1);
   bkv::RopeParams rp{};
@@ -287,7 +290,7 @@ bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache
     sp.Vc[l] = static_cast<__nv_bfloat16*>(V[l]);
   }
   sp.rows_moved = h->rows_moved();
-  sp.compact = 1;
+  sp.compact = compact;
   if (h->timed(BKV_K_SCORE, [&] { return bkv::launch_score_select(sp, h->stream); }) != cudaSuccess)
     return BKV_ERR_CUDA;
 

@@ -78,7 +78,8 @@ struct ScoreParams {
   __nv_bfloat16* Kc[kMaxLayers];
   __nv_bfloat16* Vc[kMaxLayers];
   unsigned long long* rows_moved;
-  int compact;
+  int compact;  // 0: score and keep set only; 1: compact in slot order (eq. 8);
+                // 2: order-free (holes below the budget filled from the kept tail)
 };
 cudaError_t launch_score_select(const ScoreParams& p, cudaStream_t s);
 // Dynamic shared memory the score kernel needs (huge when the shape does not fit).

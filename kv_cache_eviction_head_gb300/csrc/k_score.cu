@@ -249,7 +249,7 @@ __device__ __forceinline__ bool key_less(uint32_t ah, uint32_t al, uint32_t bh, 
   return ah < bh || (ah == bh && al < bl);
 }
 __device__ void select_keep(const float* sc, int L, int prefix, int recent, int budget, int32_t* out,
-                            uint32_t* dropped, int* drops) {
+                            uint32_t* dropped, int* drops, bool order_free) {
   const int lane = threadIdx.x & 31;
   const int c0 = prefix < L ? prefix : L;
   const int c1 = L - recent > c0 ? L - recent : c0;
@@ -323,10 +323,25 @@ __device__ void select_keep(const float* sc, int L, int prefix, int recent, int 
     const bool keep = j < L && !drop;
     const unsigned lt = (1u << lane) - 1u;
     const unsigned m = __ballot_sync(kFull, keep), dm = __ballot_sync(kFull, drop);
-    if (keep) out[base + __popc(m & lt)] = j;
+    if (keep && !order_free) out[base + __popc(m & lt)] = j;
     if (drop && drops) drops[dbase + __popc(dm & lt)] = j;
     base += __popc(m);
     dbase += __popc(dm);
+  }
+  if (order_free) {
+    // layout of the order-free compaction: slots below the budget keep their
+    // rows, except the holes (dropped, ascending), which receive the kept slots
+    // at or above the budget (ascending)
+    __syncwarp();
+    int h = 0;  // holes = dropped slots below the budget = drops[0, h)
+    for (int r0 = 0; r0 < D; r0 += 32) h += __popc(__ballot_sync(kFull, r0 + lane < D && drops[r0 + lane] < budget));
+    for (int j = lane; j < budget; j += 32)
+      if (!((dropped[j >> 5] >> (j & 31)) & 1u)) out[j] = j;
+    for (int k = lane; k < h; k += 32) {
+      int x = budget + k;  // the k-th slot >= budget that is not dropped
+      for (int r = h; r < D && drops[r] <= x; ++r) ++x;
+      out[drops[k]] = x;
+    }
   }
 }
 
@@ -345,7 +360,9 @@ struct Layout {
 // lo), the per-row statistics and tables; the rest goes to K-tile stages,
 // compaction chunks and score buffers, in the first arrangement that fits:
 // two or more K stages always, eight / four / two 8 KB compaction chunks when
-// compacting, two score buffers (one when nothing else fits).
+// compacting in slot order, two chunks (and more K stages) for the order-free
+// compaction, which moves at most L - budget rows; two score buffers (one
+// when nothing else fits).
 __host__ __device__ inline Layout make_layout(int R, int L, int nr, int budget, int compact) {
   Layout s;
   s.R = R;
@@ -364,11 +381,12 @@ __host__ __device__ inline Layout make_layout(int R, int L, int nr, int budget, 
   const size_t scb = (size_t)s.Lp * 4;
   static const int plans[][3] = {{4, 0, 2}, {3, 0, 2}, {2, 0, 2}, {2, 0, 1}};          // no compaction
   static const int cplans[][3] = {{2, 8, 2}, {2, 4, 2}, {2, 2, 2}, {2, 2, 1}};         // compaction
+  static const int oplans[][3] = {{4, 2, 2}, {3, 2, 2}, {2, 2, 2}, {2, 2, 1}};         // order-free
   s.stages = 0;
   s.cbufs = 0;
   s.scbufs = 0;
   for (int i = 0; i < 4; ++i) {
-    const int* pl = compact ? cplans[i] : plans[i];
+    const int* pl = compact == 2 ? oplans[i] : compact ? cplans[i] : plans[i];
     const size_t need = 2 * qbytes + (size_t)pl[0] * kTileBytes + (size_t)pl[1] * kChunkBytes + pl[2] * scb + small;
     if (need <= cap) {
       s.stages = pl[0];
@@ -694,6 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
         int4* cdesc = reinterpret_cast<int4*>(smem + lay.misc + 1536);  // [cbufs] tensor, source row, rows, shift
         int lb = 0, sb = 0;  // next buffer to load into / to store from (loads and stores cycle alike)
         uint32_t sph = 0;    // parity of buffer sb's next completion
+        uint32_t ofph[2] = {0u, 0u};  // order-free: parity of buffers 0 and 1's next completion
         bool ok = true;
         const uint64_t stream = policy_evict_first();
         for (int it = 0; it < mine && ok; ++it) {
@@ -706,93 +725,141 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
           const size_t rowbase = (size_t)(seq * P.kv_heads + kvh) * P.max_cache;
           char* tb[2] = {reinterpret_cast<char*>(P.Kc[layer] + rowbase * kD),
                          reinterpret_cast<char*>(P.Vc[layer] + rowbase * kD)};
-          const int first = D > 0 ? dl[0] + 1 : L;  // lowest source row that moves
-          // chunk cursor over the runs of K, then of V: tensor ct, run cr, next source row crow
-          int ct = 0, cr = 0, crow = first;
-          auto next = [&](int4& c) -> bool {
-            while (ct < 2 && D > 0) {
-              const int end = cr + 1 < D ? dl[cr + 1] : L;
-              if (crow < end) {
-                const int n = end - crow < kChunkRows ? end - crow : kChunkRows;
-                c = make_int4(ct, crow, n, cr + 1);  // run cr moves down by cr + 1 slots
-                crow += n;
-                return true;
+          unsigned long long moved = 0;  // rows moved per tensor
+          if (P.compact == 2) {
+            // Order-free compaction: the k-th dropped slot below the budget (a
+            // hole) receives the k-th kept slot at or above the budget. Sources
+            // and destinations are disjoint, so chunks need no ordering; K rows
+            // go through chunk buffer 0 and V rows through buffer 1.
+            int h = 0;
+            while (h < D && dl[h] < P.budget) ++h;
+            int2* pairs = reinterpret_cast<int2*>(smem + lay.misc + 1664);  // [kChunkRows] (source, hole)
+            int r = h, x = P.budget;  // next dropped slot at or above the budget; next tail slot
+            for (int k0 = 0; k0 < h && ok; k0 += kChunkRows) {
+              const int n = h - k0 < kChunkRows ? h - k0 : kChunkRows;
+              bulk_wait_read<0>();  // earlier stores are done reading both buffers
+              for (int i = 0; i < n; ++i) {
+                while (r < D && dl[r] == x) {
+                  ++r;
+                  ++x;
+                }
+                pairs[i] = make_int2(x++, dl[k0 + i]);
               }
-              if (++cr < D) {
-                crow = dl[cr] + 1;
-              } else {
-                ++ct;
-                cr = 0;
-                crow = first;
+              for (int t2 = 0; t2 < 2; ++t2) {
+                mbar_expect_tx(&cfull[t2], (uint32_t)n * (kD * 2));
+                for (int i = 0; i < n; ++i)
+                  bulk_load(smem_u32(cst + (size_t)t2 * kChunkBytes + (size_t)i * (kD * 2)),
+                            tb[t2] + (size_t)pairs[i].x * (kD * 2), kD * 2, &cfull[t2], stream);
               }
+              const bool w0 = mbar_wait(&cfull[0], ofph[0], ctl, P.status);
+              const bool w1 = w0 && mbar_wait(&cfull[1], ofph[1], ctl, P.status);
+              if (!w1) {  // loads already issued must land before the CTA exits
+                for (int t2 = 0; t2 < 2; ++t2) {
+                  const long long t0 = clock64();
+                  while (!mbar_test(&cfull[t2], ofph[t2]) && clock64() - t0 < kWaitCycles) {
+                  }
+                }
+                ok = false;
+                break;
+              }
+              ofph[0] ^= 1u;
+              ofph[1] ^= 1u;
+              for (int t2 = 0; t2 < 2; ++t2)
+                for (int i = 0; i < n; ++i)
+                  bulk_store(tb[t2] + (size_t)pairs[i].y * (kD * 2),
+                             smem_u32(cst + (size_t)t2 * kChunkBytes + (size_t)i * (kD * 2)), kD * 2, stream);
+              bulk_commit();
             }
-            return false;
-          };
-          // With few chunk buffers the loads alone keep too few bytes in
-          // flight to cover HBM latency; the moved rows [first, L) of K, then
-          // of V, are then prefetched into L2 kPfRows rows ahead of them.
-          const bool pf_on = CB <= 4;
-          const int moved = L - first;
-          int pf_row = 0;  // rows prefetched so far, K's moved rows then V's
-          auto prefetch_to = [&](int target) {
-            target = target < 2 * moved ? target : 2 * moved;
-            while (pf_row < target) {
-              const int pt = pf_row >= moved ? 1 : 0;
-              const int off = pf_row - (pt ? moved : 0);
-              int nr = moved - off < kPfPieceRows ? moved - off : kPfPieceRows;
-              nr = target - pf_row < nr ? target - pf_row : nr;
-              bulk_prefetch_l2(tb[pt] + (size_t)(first + off) * (kD * 2), (uint32_t)nr * (kD * 2));
-              pf_row += nr;
-            }
-          };
-          if (pf_on) prefetch_to(kPfRows);
-          auto load = [&](const int4& c) {
-            cdesc[lb] = c;
-            const uint32_t bytes = (uint32_t)c.z * (kD * 2);
-            mbar_expect_tx(&cfull[lb], bytes);
-            bulk_load(smem_u32(cst + (size_t)lb * kChunkBytes), tb[c.x] + (size_t)c.y * (kD * 2), bytes, &cfull[lb],
-                      stream);
-            lb = lb + 1 == CB ? 0 : lb + 1;
-            if (pf_on) prefetch_to((c.x ? moved : 0) + c.y + c.z - first + kPfRows);
-          };
-          bulk_wait_read<0>();  // the previous unit's stores are done reading every chunk buffer
-          int inflight = 0;
-          int4 c;
-          while (inflight < CB - 1 && next(c)) {
-            load(c);
-            ++inflight;
-          }
-          while (inflight > 0) {
-            ok = mbar_wait(&cfull[sb], sph, ctl, P.status);
-            if (!ok) break;
-            const int4 d = cdesc[sb];
-            bulk_store(tb[d.x] + (size_t)(d.y - d.w) * (kD * 2), smem_u32(cst + (size_t)sb * kChunkBytes),
-                       (uint32_t)d.z * (kD * 2), stream);
-            bulk_commit();
-            if (++sb == CB) {
-              sb = 0;
-              sph ^= 1u;
-            }
-            --inflight;
-            if (next(c)) {
-              bulk_wait_read<1>();  // the buffer reused now belonged to the store before the last one
+            moved = (unsigned long long)h;
+          } else {
+            const int first = D > 0 ? dl[0] + 1 : L;  // lowest source row that moves
+            // chunk cursor over the runs of K, then of V: tensor ct, run cr, next source row crow
+            int ct = 0, cr = 0, crow = first;
+            auto next = [&](int4& c) -> bool {
+              while (ct < 2 && D > 0) {
+                const int end = cr + 1 < D ? dl[cr + 1] : L;
+                if (crow < end) {
+                  const int n = end - crow < kChunkRows ? end - crow : kChunkRows;
+                  c = make_int4(ct, crow, n, cr + 1);  // run cr moves down by cr + 1 slots
+                  crow += n;
+                  return true;
+                }
+                if (++cr < D) {
+                  crow = dl[cr] + 1;
+                } else {
+                  ++ct;
+                  cr = 0;
+                  crow = first;
+                }
+              }
+              return false;
+            };
+            // With few chunk buffers the loads alone keep too few bytes in
+            // flight to cover HBM latency; the moved rows [first, L) of K, then
+            // of V, are then prefetched into L2 kPfRows rows ahead of them.
+            const bool pf_on = CB <= 4;
+            const int span = L - first;
+            int pf_row = 0;  // rows prefetched so far, K's moved rows then V's
+            auto prefetch_to = [&](int target) {
+              target = target < 2 * span ? target : 2 * span;
+              while (pf_row < target) {
+                const int pt = pf_row >= span ? 1 : 0;
+                const int off = pf_row - (pt ? span : 0);
+                int nr = span - off < kPfPieceRows ? span - off : kPfPieceRows;
+                nr = target - pf_row < nr ? target - pf_row : nr;
+                bulk_prefetch_l2(tb[pt] + (size_t)(first + off) * (kD * 2), (uint32_t)nr * (kD * 2));
+                pf_row += nr;
+              }
+            };
+            if (pf_on) prefetch_to(kPfRows);
+            auto load = [&](const int4& c) {
+              cdesc[lb] = c;
+              const uint32_t bytes = (uint32_t)c.z * (kD * 2);
+              mbar_expect_tx(&cfull[lb], bytes);
+              bulk_load(smem_u32(cst + (size_t)lb * kChunkBytes), tb[c.x] + (size_t)c.y * (kD * 2), bytes, &cfull[lb],
+                        stream);
+              lb = lb + 1 == CB ? 0 : lb + 1;
+              if (pf_on) prefetch_to((c.x ? span : 0) + c.y + c.z - first + kPfRows);
+            };
+            bulk_wait_read<0>();  // the previous unit's stores are done reading every chunk buffer
+            int inflight = 0;
+            int4 c;
+            while (inflight < CB - 1 && next(c)) {
               load(c);
               ++inflight;
             }
-          }
-          if (!ok) {  // after an abort, loads already issued must land before the CTA exits
-            for (; inflight > 0; --inflight) {
-              const long long t0 = clock64();
-              while (!mbar_test(&cfull[sb], sph) && clock64() - t0 < kWaitCycles) {
-              }
+            while (inflight > 0) {
+              ok = mbar_wait(&cfull[sb], sph, ctl, P.status);
+              if (!ok) break;
+              const int4 d = cdesc[sb];
+              bulk_store(tb[d.x] + (size_t)(d.y - d.w) * (kD * 2), smem_u32(cst + (size_t)sb * kChunkBytes),
+                         (uint32_t)d.z * (kD * 2), stream);
+              bulk_commit();
               if (++sb == CB) {
                 sb = 0;
                 sph ^= 1u;
               }
+              --inflight;
+              if (next(c)) {
+                bulk_wait_read<1>();  // the buffer reused now belonged to the store before the last one
+                load(c);
+                ++inflight;
+              }
             }
+            if (!ok) {  // after an abort, loads already issued must land before the CTA exits
+              for (; inflight > 0; --inflight) {
+                const long long t0 = clock64();
+                while (!mbar_test(&cfull[sb], sph) && clock64() - t0 < kWaitCycles) {
+                }
+                if (++sb == CB) {
+                  sb = 0;
+                  sph ^= 1u;
+                }
+              }
+            }
+            moved = D > 0 ? (unsigned long long)(L - D - dl[0]) : 0ull;
           }
-          if (ok && D > 0 && P.rows_moved)
-            atomicAdd(P.rows_moved, (unsigned long long)(L - D - dl[0]));
+          if (ok && moved && P.rows_moved) atomicAdd(P.rows_moved, moved);
           mbar_arrive(&dfree[b]);
         }
         bulk_wait_all();  // every store has landed before the CTA may exit
@@ -828,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       for (int j = lane; j < L; j += 32) bad |= s_u[j] != s_u[j];
       if (__any_sync(kFull, bad) && lane == 0) latch(P.status, BKV_ERR_NONFINITE);
       select_keep(s_u, L, P.prefix, P.recent, P.budget, P.kept + (size_t)u * P.budget, dropbits,
-                  P.compact ? dlist + db * lay.D : nullptr);
+                  P.compact ? dlist + db * lay.D : nullptr, P.compact == 2);
       if (P.scores) {
         float* so = P.scores + (size_t)u * P.max_cache;
         for (int j = lane; j < L; j += 32) so[j] = s_u[j];

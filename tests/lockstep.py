@@ -13,6 +13,8 @@ Agreement rules (per unit and eviction):
     byte, under the keep set the GPU returned once it passed the rule above
     (the oracle continues from that keep set so that an accepted choice inside
     the tie band does not make later rounds diverge);
+  * order-free compaction (order_free=True): the returned layout is exactly the
+    oracle's order_free_layout of the returned set, and K/V follow it;
   * FPS traces after the eviction: identical pick order for every query head.
 """
 
@@ -23,7 +25,7 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-from oracle import UnitOracle, select_keep
+from oracle import UnitOracle, order_free_layout, select_keep
 from synth import SyntheticStream, Workload, to_bits
 
 SCORE_RTOL = 2e-3
@@ -64,7 +66,7 @@ def check_keep_set(gpu_kept, s_orc, orc_kept, L, prefix, recent, budget):
 
 def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "cpu",
                  steps: int | None = None, max_failures: int = 20,
-                 query_hook=None) -> LockstepReport:
+                 query_hook=None, order_free: bool = False) -> LockstepReport:
     from kv_cache_eviction_head_gb300 import bkv
 
     dev = torch.device("cuda")
@@ -79,14 +81,16 @@ def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "c
                           period=w.period, prefix=w.prefix, recent=w.recent, fps_cap=w.fps_cap,
                           fps_keep=w.fps_keep, layers=w.layers, batch=w.batch,
                           max_cache=w.max_cache, rope_theta=w.theta,
-                          flags=bkv.BKV_FLAG_KEEP_SCORES)
+                          flags=bkv.BKV_FLAG_KEEP_SCORES
+                          | (bkv.BKV_FLAG_ORDER_FREE if order_free else 0))
     ws = torch.empty(bkv.bkv_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
     h = bkv.bkv_create(cfg, ws, torch.cuda.current_stream())
 
     if sample_units is None:
         sample_units = [(l, b, kh) for l in range(w.layers) for b in range(w.batch)
                         for kh in range(w.kv_heads)]
-    oracles = {u: UnitOracle(G, d, w.theta, w.budget, w.prefix, w.recent, w.fps_cap, w.fps_keep)
+    oracles = {u: UnitOracle(G, d, w.theta, w.budget, w.prefix, w.recent, w.fps_cap, w.fps_keep,
+                             order_free=order_free)
                for u in sample_units}
     live = set(sample_units)
     idx_dev = torch.device(gen_device)
@@ -160,8 +164,11 @@ def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "c
                     live.discard((l, b, kh))
                     continue
                 orc_kept = select_keep(s_orc, L, w.prefix, w.recent, w.budget)
-                g_kept = kept_h[l, b, kh].tolist()
+                g_layout = kept_h[l, b, kh].tolist()
+                g_kept = sorted(g_layout) if order_free else g_layout
                 why = check_keep_set(g_kept, s_orc, orc_kept, L, w.prefix, w.recent, w.budget)
+                if not why and order_free and g_layout != order_free_layout(g_kept, w.budget):
+                    why = "order-free layout differs from the holes-from-the-tail rule"
                 if why:
                     fail(f"t={t} unit {(l, b, kh)}: {why}")
                     live.discard((l, b, kh))

@@ -58,6 +58,8 @@ def test_workspace_bytes_matches_the_layout(bkv):
     assert bkv.bkv_workspace_bytes(c) == want
     c2 = cfg_for(bkv, flags=bkv.BKV_FLAG_KEEP_SCORES)
     assert bkv.bkv_workspace_bytes(c2) == want + 36 * 192 * 8 * 2064 * 4
+    c3 = cfg_for(bkv, flags=bkv.BKV_FLAG_ORDER_FREE)   # the compaction layout needs no state
+    assert bkv.bkv_workspace_bytes(c3) == want
 
 
 @pytest.mark.parametrize("over,code", [

@@ -109,6 +109,68 @@ def test_r1_qwen7b_b128_full_size_sampled_units(budget):
     assert rep.units_checked == len(units) * rep.evictions
 
 
+# ---------------------------------------------------------------------------- order-free compaction
+
+@pytest.mark.parametrize("name,over", [
+    ("base", dict()),
+    ("long_period", dict(period=24)),
+    ("no_prefix_no_recent", dict(prefix=0, recent=0)),
+    ("gqa7", dict(heads=7, kv_heads=1)),
+    ("ragged_budget", dict(budget=200, steps=300)),
+    ("batch_layers", dict(layers=2, batch=3, heads=8, kv_heads=2, steps=200)),
+])
+def test_order_free_tiny_variants(name, over):
+    """Order-free compaction over whole tiny streams: the same keep sets as the
+    oracle, the holes-from-the-tail layout, byte-exact K/V, and every later
+    eviction (which scores the scrambled slots) still matching."""
+    w = TINY.with_(**over)
+    rep = run_lockstep(w, seed=0xBEAC5, order_free=True)
+    assert_clean(rep, min_evictions=3)
+
+
+def test_order_free_qwen3_4b_b192_full_size_sampled_units():
+    w = WORKLOADS["qwen3_4b_b192"]
+    units = [(0, 0, 0), (3, 191, 7), (17, 100, 5), (35, 150, 6), (8, 1, 1)]
+    rep = run_lockstep(w, seed=0xBEAC6, sample_units=units, gen_device="cuda",
+                       steps=w.max_cache + 2 * w.period, order_free=True)
+    assert_clean(rep, min_evictions=3)
+    assert rep.units_checked == len(units) * rep.evictions
+
+
+def test_order_free_r1_qwen7b_b128_k4096_full_size_sampled_units():
+    w = WORKLOADS["r1_qwen7b_b128_k4096"]
+    units = [(0, 0, 0), (27, 127, 3), (13, 64, 1)]
+    rep = run_lockstep(w, seed=0xBEAC7, sample_units=units, gen_device="cuda",
+                       steps=w.max_cache + 2 * w.period, order_free=True)
+    assert_clean(rep, min_evictions=3)
+
+
+def test_order_free_needs_recent_window_inside_the_tail():
+    from kv_cache_eviction_head_gb300 import bkv
+    w = TINY
+    dev = torch.device("cuda")
+    cfg = bkv.make_config(heads=4, kv_heads=1, d=128, budget=w.budget, period=8, prefix=4,
+                          recent=16, layers=1, batch=1, max_cache=w.max_cache, rope_theta=1e6,
+                          flags=bkv.BKV_FLAG_ORDER_FREE)
+    ws = torch.empty(bkv.bkv_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    h = bkv.bkv_create(cfg, ws, torch.cuda.current_stream())
+    q = torch.randn(1, 1, 4, 128, device=dev).to(torch.bfloat16)
+    K = [torch.zeros(1, 1, w.max_cache, 128, dtype=torch.bfloat16, device=dev)]
+    kept = torch.empty(1, 1, 1, w.budget, dtype=torch.int32, device=dev)
+    try:
+        for t in range(w.budget + 8):
+            bkv.bkv_append_queries(h, q, t)
+        with pytest.raises(bkv.BkvError) as e:           # recent 16 > cache_len - budget = 8
+            bkv.bkv_evict(h, K, K, w.budget + 8, w.budget + 7, kept)
+        assert e.value.code == bkv.BKV_ERR_INVALID_ARG
+        for t in range(w.budget + 8, w.budget + 16):
+            bkv.bkv_append_queries(h, q, t)
+        bkv.bkv_evict(h, K, K, w.budget + 16, w.budget + 15, kept)  # recent 16 <= 16: accepted
+        bkv.bkv_sync(h)
+    finally:
+        bkv.bkv_destroy(h)
+
+
 def wide_queries(t, q):
     """Replaces some queries by vectors whose exponents span far more than 20
     binades (FPS's wide exact-sum path), by zero rows and by exact duplicates."""
