@@ -236,103 +236,132 @@ __device__ __forceinline__ float fast_log2(float x) {
   return y;
 }
 
-// Keep set of one unit from its scores sc[0, L), written ascending to out. One
-// warp. The D = L - budget dropped slots are the D smallest keys
-// (score bits, ~slot) among the candidates [prefix, L - recent): lower score
-// first, and among equal scores the higher slot first, so the lower slot wins
-// a tie. Each lane keeps the kList smallest keys of its own candidates; the
-// warp extracts the global minimum D times, and a lane whose list runs dry
-// rescans for the keys above the last one it gave up. dropped[] is a bitmask
-// over slots in shared memory.
+// Keep set of one unit from its scores sc[0, L). One warp. The D = L - budget
+// dropped slots are the D smallest 64-bit keys (score bits << 32 | ~slot)
+// among the candidates [prefix, L - recent): lower score first, and among
+// equal scores the higher slot first, so the lower slot wins a tie (scores
+// are >= 0, so their bit patterns order like the values). Each lane keeps the
+// kList smallest keys of its own candidates, built without data-dependent
+// branches: batches of 8 keys are sorted by Batcher's odd-even network and
+// merged into the list by a bitonic half-cleaner. The warp then extracts the
+// global minimum D times; a lane whose list runs dry rebuilds it from the
+// keys above the last one it gave up. dropped[] is a bitmask over slots;
+// drops[] receives the dropped slots ascending. out[] receives the kept
+// slots ascending, or with order_free the layout of the order-free
+// compaction. Returns true if a score was NaN.
 constexpr int kList = 8;
-__device__ __forceinline__ bool key_less(uint32_t ah, uint32_t al, uint32_t bh, uint32_t bl) {
-  return ah < bh || (ah == bh && al < bl);
+typedef unsigned long long u64;
+constexpr u64 kNoKey = ~0ull;
+
+__device__ __forceinline__ void cswap(u64& a, u64& b) {
+  const u64 lo = a < b ? a : b, hi = a < b ? b : a;
+  a = lo;
+  b = hi;
 }
-__device__ void select_keep(const float* sc, int L, int prefix, int recent, int budget, int32_t* out,
+__device__ __forceinline__ void sort8(u64 (&k)[8]) {
+  cswap(k[0], k[1]); cswap(k[2], k[3]); cswap(k[4], k[5]); cswap(k[6], k[7]);
+  cswap(k[0], k[2]); cswap(k[1], k[3]); cswap(k[4], k[6]); cswap(k[5], k[7]);
+  cswap(k[1], k[2]); cswap(k[5], k[6]);
+  cswap(k[0], k[4]); cswap(k[1], k[5]); cswap(k[2], k[6]); cswap(k[3], k[7]);
+  cswap(k[2], k[4]); cswap(k[3], k[5]);
+  cswap(k[1], k[2]); cswap(k[3], k[4]); cswap(k[5], k[6]);
+}
+// list <- the 8 smallest of list and k, both sorted ascending
+__device__ __forceinline__ void merge8(u64 (&list)[8], const u64 (&k)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) list[i] = list[i] < k[7 - i] ? list[i] : k[7 - i];  // bitonic
+#pragma unroll
+  for (int dd = 4; dd > 0; dd >>= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((i & dd) == 0) cswap(list[i], list[i + dd]);
+}
+
+__device__ bool select_keep(const float* sc, int L, int prefix, int recent, int budget, int32_t* out,
                             uint32_t* dropped, int* drops, bool order_free) {
+  static_assert(kList == 8, "the list networks are written for 8 keys");
   const int lane = threadIdx.x & 31;
   const int c0 = prefix < L ? prefix : L;
   const int c1 = L - recent > c0 ? L - recent : c0;
   const int D = L - budget;
-  const uint32_t none = 0xFFFFFFFFu;
   for (int wd = lane; wd < (L + 31) / 32; wd += 32) dropped[wd] = 0u;
-  // lane-local sorted lists of (hi = score bits, lo = ~slot)
-  uint32_t lh[kList], ll[kList];
-  auto fill = [&](uint32_t after_h, uint32_t after_l) {
+  u64 list[kList];
+  bool bad = false;
+  // the lane's kList smallest keys above `after`
+  auto fill = [&](u64 after) {
 #pragma unroll
-    for (int i = 0; i < kList; ++i) {
-      lh[i] = none;
-      ll[i] = none;
-    }
-    for (int j = c0 + lane; j < c1; j += 32) {
-      const uint32_t kh = __float_as_uint(sc[j]), kl = ~(uint32_t)j;
-      if (!key_less(after_h, after_l, kh, kl)) continue;  // already given up
-      if (!key_less(kh, kl, lh[kList - 1], ll[kList - 1])) continue;
-      uint32_t ch = kh, cl = kl;
+    for (int i = 0; i < kList; ++i) list[i] = kNoKey;
+    for (int j0 = c0 + lane; j0 < c1; j0 += 32 * 8) {
+      u64 k[8];
 #pragma unroll
-      for (int i = 0; i < kList; ++i) {  // insertion into the sorted list
-        if (key_less(ch, cl, lh[i], ll[i])) {
-          const uint32_t th = lh[i], tl = ll[i];
-          lh[i] = ch;
-          ll[i] = cl;
-          ch = th;
-          cl = tl;
+      for (int i = 0; i < 8; ++i) {
+        const int j = j0 + 32 * i;
+        k[i] = kNoKey;
+        if (j < c1) {
+          const float v = sc[j];
+          bad |= v != v;
+          const u64 key = ((u64)__float_as_uint(v) << 32) | (uint32_t)~j;
+          if (key > after) k[i] = key;
         }
       }
+      sort8(k);
+      if (k[0] < list[kList - 1]) merge8(list, k);
     }
   };
-  fill(0u, 0u);
-  // (0, 0) precedes every real key except score 0 at slot 0xFFFFFFFF, which cannot occur
-  uint32_t last_h = 0u, last_l = 0u;
+  fill(0ull);  // no real key is 0: that needs slot 0xFFFFFFFF
   int used = 0;
   __syncwarp();
   for (int d = 0; d < D; ++d) {
-    uint32_t mh = lh[0], ml = ll[0];
+    u64 m = list[0];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      const uint32_t oh = __shfl_xor_sync(kFull, mh, off), ol = __shfl_xor_sync(kFull, ml, off);
-      if (key_less(oh, ol, mh, ml)) {
-        mh = oh;
-        ml = ol;
-      }
+      const u64 o = __shfl_xor_sync(kFull, m, off);
+      m = o < m ? o : m;
     }
-    const int slot = (int)(~ml);
+    const int slot = (int)(~(uint32_t)m);
     if (lane == 0) atomicOr(&dropped[slot >> 5], 1u << (slot & 31));
-    if (lh[0] == mh && ll[0] == ml) {  // this lane owned it: pop, refill when empty
-      last_h = mh;
-      last_l = ml;
+    if (list[0] == m) {  // this lane owned it: pop, rebuild when empty
 #pragma unroll
-      for (int i = 0; i < kList - 1; ++i) {
-        lh[i] = lh[i + 1];
-        ll[i] = ll[i + 1];
-      }
-      lh[kList - 1] = none;
-      ll[kList - 1] = none;
+      for (int i = 0; i < kList - 1; ++i) list[i] = list[i + 1];
+      list[kList - 1] = kNoKey;
       if (++used == kList) {
-        fill(last_h, last_l);
+        fill(m);
         used = 0;
       }
     }
   }
   __syncwarp();
-  // kept slots in ascending order, written 32 at a time; dropped slots likewise
-  int base = 0, dbase = 0;
-  for (int j0 = 0; j0 < L; j0 += 32) {
-    const int j = j0 + lane;
-    const bool drop = j < L && ((dropped[j >> 5] >> (j & 31)) & 1u);
-    const bool keep = j < L && !drop;
-    const unsigned lt = (1u << lane) - 1u;
-    const unsigned m = __ballot_sync(kFull, keep), dm = __ballot_sync(kFull, drop);
-    if (keep && !order_free) out[base + __popc(m & lt)] = j;
-    if (drop && drops) drops[dbase + __popc(dm & lt)] = j;
-    base += __popc(m);
-    dbase += __popc(dm);
+  // dropped slots ascending: per-word counts, a warp prefix sum, then the bits
+  const int words = (L + 31) / 32;
+  int dbase = 0;
+  for (int w0 = 0; w0 < words; w0 += 32) {
+    const int w = w0 + lane;
+    uint32_t bits = w < words ? dropped[w] : 0u;
+    const int c = __popc(bits);
+    int x = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(kFull, x, off);
+      if (lane >= off) x += y;
+    }
+    int pos = dbase + x - c;
+    while (bits) {
+      drops[pos++] = w * 32 + __ffs(bits) - 1;
+      bits &= bits - 1;
+    }
+    dbase += __shfl_sync(kFull, x, 31);
   }
-  if (order_free) {
+  __syncwarp();
+  if (!order_free) {
+    // kept slots ascending, run by run: slot s between drops r-1 and r goes to out[s - r]
+    for (int r = 0; r <= D; ++r) {
+      const int s0 = r == 0 ? 0 : drops[r - 1] + 1, s1 = r == D ? L : drops[r];
+      for (int s = s0 + lane; s < s1; s += 32) out[s - r] = s;
+    }
+  } else {
     // layout of the order-free compaction: slots below the budget keep their
     // rows, except the holes (dropped, ascending), which receive the kept slots
     // at or above the budget (ascending)
-    __syncwarp();
     int h = 0;  // holes = dropped slots below the budget = drops[0, h)
     for (int r0 = 0; r0 < D; r0 += 32) h += __popc(__ballot_sync(kFull, r0 + lane < D && drops[r0 + lane] < budget));
     for (int j = lane; j < budget; j += 32)
@@ -343,6 +372,7 @@ __device__ void select_keep(const float* sc, int L, int prefix, int recent, int 
       out[drops[k]] = x;
     }
   }
+  return __any_sync(kFull, bad);
 }
 
 constexpr int kChunkRows = 32;                   // rows per compaction chunk
@@ -376,7 +406,7 @@ __host__ __device__ inline Layout make_layout(int R, int L, int nr, int budget, 
   s.D = L - budget;
   const size_t qbytes = ((size_t)s.qrows * 256 + 1023) / 1024 * 1024;  // two 128-byte slabs per row
   const size_t small = (size_t)s.rows64 * 8 + (size_t)s.qrows * 16 + (size_t)s.qrows * 8 +
-                       (compact ? 2 * (size_t)s.D * 4 + 16 : 0) + 64 * 8 + 2048 + 64;
+                       2 * (size_t)s.D * 4 + 16 + 64 * 8 + 2048 + 64;
   const size_t cap = 227 * 1024 - 1024;  // 1 KB kept for aligning the dynamic base
   const size_t scb = (size_t)s.Lp * 4;
   static const int plans[][3] = {{4, 0, 2}, {3, 0, 2}, {2, 0, 2}, {2, 0, 1}};          // no compaction
@@ -415,7 +445,7 @@ __host__ __device__ inline Layout make_layout(int R, int L, int nr, int budget, 
   s.rowinfo = off;
   off += (size_t)s.qrows * 8;
   s.drops = off;
-  off += compact ? 2 * (size_t)s.D * 4 + 16 : 0;
+  off += 2 * (size_t)s.D * 4 + 16;
   s.bars = (off + 7) & ~(size_t)7;
   off = s.bars + 64 * 8;
   s.misc = off;
@@ -891,11 +921,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       if (!ok) break;
       const int u = blockIdx.x + it * gridDim.x;
       const float* s_u = sc + (size_t)b * lay.Lp;
-      bool bad = false;
-      for (int j = lane; j < L; j += 32) bad |= s_u[j] != s_u[j];
-      if (__any_sync(kFull, bad) && lane == 0) latch(P.status, BKV_ERR_NONFINITE);
-      select_keep(s_u, L, P.prefix, P.recent, P.budget, P.kept + (size_t)u * P.budget, dropbits,
-                  P.compact ? dlist + db * lay.D : nullptr, P.compact == 2);
+      const bool bad = select_keep(s_u, L, P.prefix, P.recent, P.budget, P.kept + (size_t)u * P.budget,
+                                   dropbits, dlist + db * lay.D, P.compact == 2);
+      if (bad && lane == 0) latch(P.status, BKV_ERR_NONFINITE);
       if (P.scores) {
         float* so = P.scores + (size_t)u * P.max_cache;
         for (int j = lane; j < L; j += 32) so[j] = s_u[j];
