@@ -24,6 +24,7 @@ from .beaconkv import (
     fps,
     attention_weights,
     max_pool,
+    mean_pool,
     select_keep,
     order_free_layout,
     UnitOracle,
@@ -31,5 +32,5 @@ from .beaconkv import (
 
 __all__ = [
     "bf16_to_f64", "rope", "exact_dot", "gram_exact", "cosine_matrix", "fps",
-    "attention_weights", "max_pool", "select_keep", "order_free_layout", "UnitOracle",
+    "attention_weights", "max_pool", "mean_pool", "select_keep", "order_free_layout", "UnitOracle",
 ]

@@ -181,6 +181,15 @@ def max_pool(W) -> np.ndarray:
     return np.asarray(W).max(axis=0)
 
 
+def mean_pool(W) -> np.ndarray:
+    """Score[j] = the mean of W[., j] over every observation row, the mean
+    aggregation of BeaconKV reading notes §2.1 eq. 6 applied over queries and
+    heads together (Table 2 compares the two aggregations over both at once).
+    Inaccessible entries are 0 and count in the denominator."""
+    W = np.asarray(W, dtype=np.float64)
+    return W.sum(axis=0) / W.shape[0]
+
+
 # ----------------------------------------------------------------------------
 # keep set and compaction (BeaconKV reading notes, §2.3 eq. 8)
 
@@ -255,12 +264,16 @@ class UnitOracle:
                     Bq <- FPS(Bq + R, fps_keep) and R <- empty (Algorithm 2).
     With order_free, the compaction keeps the same set but in the layout of
     order_free_layout (holes below the budget filled from the tail); keys
-    carry their positions, so later masking is unchanged.
+    carry their positions, so later masking is unchanged. pool = "mean"
+    scores with mean_pool instead of max_pool (Table 2's ablation).
     """
 
     def __init__(self, group: int, d: int, theta: float, budget: int, prefix: int,
-                 recent: int, fps_cap: int, fps_keep: int, order_free: bool = False):
+                 recent: int, fps_cap: int, fps_keep: int, order_free: bool = False,
+                 pool: str = "max"):
+        assert pool in ("max", "mean")
         self.order_free = order_free
+        self.pool = pool
         self.group, self.d, self.theta = group, d, theta
         self.budget, self.prefix, self.recent = budget, prefix, recent
         self.fps_cap, self.fps_keep = fps_cap, fps_keep
@@ -306,7 +319,7 @@ class UnitOracle:
         if Q.shape[0] == 0:
             return np.zeros(L), 0
         W = attention_weights(Q, qpos, bf16_to_f64(np.stack(self.K)), np.asarray(self.pos))
-        return max_pool(W), Q.shape[0]
+        return (mean_pool(W) if self.pool == "mean" else max_pool(W)), Q.shape[0]
 
     def evict(self, t: int, kept_override=None, score=None) -> EvictResult:
         """One eviction at time t. `kept_override`, when given, is a keep set the

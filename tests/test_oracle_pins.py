@@ -18,7 +18,7 @@ import pytest
 import torch
 
 from oracle import (UnitOracle, attention_weights, bf16_to_f64, cosine_matrix, exact_dot, fps,
-                    gram_exact, max_pool, order_free_layout, rope, select_keep)
+                    gram_exact, max_pool, mean_pool, order_free_layout, rope, select_keep)
 from synth import kv_bytes_per_token, to_bits
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -312,6 +312,63 @@ def test_zero_beacons_reduce_to_snapkv_max_formula():
                                     bf16_to_f64(np.stack(u.K)), u.pos, 1e6, d)
             assert np.allclose(got, want, rtol=1e-12, atol=0)
         u.evict(t - 1)
+
+
+def snapkv_mean_score(heads_recent, K_vals, k_pos, theta, d):
+    """Recent-window mean score (eq. 6 of the notes) averaged over the query
+    heads of the group as well, written as explicit loops: every observation
+    row contributes its softmax weight (0 for keys it cannot access)."""
+    L = len(K_vals)
+    total = [0.0] * L
+    rows = 0
+    for recent in heads_recent:
+        for q, tau in recent:
+            rows += 1
+            qr = rope(bf16_to_f64(q), tau, theta)
+            acc = [j for j in range(L) if k_pos[j] <= tau]
+            logit = {j: float(qr @ K_vals[j]) / math.sqrt(d) for j in acc}
+            mx = max(logit.values())
+            z = math.fsum(math.exp(v - mx) for v in logit.values())
+            for j in acc:
+                total[j] += math.exp(logit[j] - mx) / z
+    return np.array(total) / rows
+
+
+def test_mean_pool_zero_beacons_is_the_recent_window_mean_formula():
+    G, d = 2, 128
+    u = UnitOracle(group=G, d=d, theta=1e6, budget=40, prefix=4, recent=8, fps_cap=16,
+                   fps_keep=0, pool="mean")
+    g = torch.Generator().manual_seed(12)
+    t = 0
+    for rnd in range(2):
+        while len(u.K) < 56:
+            u.append_kv(to_bits(torch.randn(d, generator=g).to(torch.bfloat16)),
+                        to_bits(torch.randn(d, generator=g).to(torch.bfloat16)), t)
+            u.append_queries(to_bits(torch.randn(G, d, generator=g).to(torch.bfloat16)), t)
+            t += 1
+        if rnd == 1:
+            got, nobs = u.scores(t - 1)
+            want = snapkv_mean_score([list(st.rq) for st in u.heads],
+                                     bf16_to_f64(np.stack(u.K)), u.pos, 1e6, d)
+            assert nobs == G * 16
+            assert np.allclose(got, want, rtol=1e-12, atol=0)
+        u.evict(t - 1)
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_mean_pool_scores_sum_to_one_and_bound_the_max(seed):
+    """Each softmax row sums to 1 over its accessible keys, so the mean over
+    rows sums to 1 over the cache; the mean never exceeds the max, and with
+    one row the two poolings coincide."""
+    g = np.random.default_rng(seed)
+    R, L, d = int(g.integers(1, 12)), int(g.integers(5, 60)), 16
+    Q, K = g.standard_normal((R, d)), g.standard_normal((L, d))
+    qpos = g.integers(L // 2, L, size=R)
+    W = attention_weights(Q, qpos, K, np.arange(L))
+    mp = mean_pool(W)
+    assert math.isclose(float(mp.sum()), 1.0, rel_tol=1e-12)
+    assert np.all(mp <= max_pool(W) + 1e-15)
+    assert np.allclose(mean_pool(W[:1]), max_pool(W[:1]), rtol=0, atol=0)
 
 
 # ---------------------------------------------------------------------------- keep set
