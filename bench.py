@@ -275,7 +275,8 @@ def run_ours(args, w):
                           period=w.period, prefix=w.prefix, recent=w.recent, fps_cap=w.fps_cap,
                           fps_keep=w.fps_keep, layers=w.layers, batch=w.batch,
                           max_cache=w.max_cache, rope_theta=w.theta,
-                          flags=bkv.BKV_FLAG_ORDER_FREE if args.order_free else 0)
+                          flags=(bkv.BKV_FLAG_ORDER_FREE if args.order_free else 0)
+                          | (bkv.BKV_FLAG_MEAN_POOL if args.pool == "mean" else 0))
     ws = torch.empty(bkv.bkv_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
     cs = torch.cuda.current_stream(dev)
     h = bkv.bkv_create(cfg, ws, cs)
@@ -409,7 +410,8 @@ def run_ours(args, w):
                            2 * w.layers * w.batch * w.kv_heads * w.max_cache * w.d * 2 / 1e9),
                        "step": f"1 eviction + {w.period} query appends",
                        "compaction": "order-free (holes filled from the kept tail)" if args.order_free
-                       else "slot order (eq. 8)"},
+                       else "slot order (eq. 8)",
+                       "pooling": args.pool},
             "gpu_launches": int(sum(n for _, n in ktimes.values())),
             "roofline": roofline,
             "path": {"alg_bytes_per_step": pbytes,
@@ -506,6 +508,10 @@ def main():
     ap.add_argument("--ref-units-per-step", type=int, default=32)
     ap.add_argument("--order-free", action="store_true",
                     help="order-free compaction (BKV_FLAG_ORDER_FREE) instead of slot order")
+    ap.add_argument("--pool", choices=["max", "mean"], default="max",
+                    help="aggregation of the attention weights over observation rows")
+    ap.add_argument("--fps-keep", type=int, default=None,
+                    help="beacons kept per head (recent queries = 32 - this), Table 1's splits")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
@@ -515,6 +521,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.batch:
         w = w.with_(batch=args.batch, name=f"{w.name}_batch{args.batch}")
+    if args.fps_keep is not None:
+        w = w.with_(fps_keep=args.fps_keep, name=f"{w.name}_keep{args.fps_keep}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

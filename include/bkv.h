@@ -69,6 +69,11 @@ typedef enum bkv_status {
  * stay in position order, which the next eviction's recent window and causal
  * mask rely on, so bkv_evict requires recent <= cache_len - budget. */
 #define BKV_FLAG_ORDER_FREE 2
+/* Mean pooling: Score[j] = the mean over all G * (beacons + recents)
+ * observation rows of their attention weight on slot j (0 where a recent row
+ * cannot see j), instead of the max (notes §2.1 eq. 6, the aggregation Table 2
+ * compares with max pooling over queries and heads). */
+#define BKV_FLAG_MEAN_POOL 4
 
 typedef struct bkv_config {
   int32_t heads;      /* query heads per layer, H                                   */

@@ -31,6 +31,7 @@ BKV_ERR_UNSUPPORTED = 7
 BKV_ERR_INTERNAL = 8
 BKV_FLAG_KEEP_SCORES = 1
 BKV_FLAG_ORDER_FREE = 2
+BKV_FLAG_MEAN_POOL = 4
 
 EXPORTED = ["bkv_workspace_bytes", "bkv_create", "bkv_set_stream", "bkv_append_queries",
             "bkv_evict", "bkv_sync", "bkv_get_fps_trace", "bkv_get_scores", "bkv_get_head_state",

@@ -33,7 +33,7 @@ bkv_status check_config(const bkv_config* c) {
   if (c->fps_cap <= 0 || c->fps_keep < 0 || c->fps_keep >= c->fps_cap) return BKV_ERR_INVALID_ARG;
   if (c->layers <= 0 || c->batch <= 0 || c->max_cache <= c->budget) return BKV_ERR_INVALID_ARG;
   if (!(c->rope_theta > 0.0)) return BKV_ERR_INVALID_ARG;
-  if (c->flags & ~(BKV_FLAG_KEEP_SCORES | BKV_FLAG_ORDER_FREE)) return BKV_ERR_INVALID_ARG;
+  if (c->flags & ~(BKV_FLAG_KEEP_SCORES | BKV_FLAG_ORDER_FREE | BKV_FLAG_MEAN_POOL)) return BKV_ERR_INVALID_ARG;
   if (c->d != bkv::kD || c->fps_cap > bkv::kMaxFpsCap || c->layers > bkv::kMaxLayers)
     return BKV_ERR_UNSUPPORTED;
   const int64_t units = (int64_t)c->layers * c->batch * c->kv_heads;
@@ -291,6 +291,7 @@ bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache
   }
   sp.rows_moved = h->rows_moved();
   sp.compact = compact;
+  sp.pool_mean = (c.flags & BKV_FLAG_MEAN_POOL) ? 1 : 0;
   if (h->timed(BKV_K_SCORE, [&] { return bkv::launch_score_select(sp, h->stream); }) != cudaSuccess)
     return BKV_ERR_CUDA;
 

@@ -80,6 +80,7 @@ struct ScoreParams {
   unsigned long long* rows_moved;
   int compact;  // 0: score and keep set only; 1: compact in slot order (eq. 8);
                 // 2: order-free (holes below the budget filled from the kept tail)
+  int pool_mean;  // 1: Score[j] = mean over the observation rows of W[., j] (Table 2)
 };
 cudaError_t launch_score_select(const ScoreParams& p, cudaStream_t s);
 // Dynamic shared memory the score kernel needs (huge when the shape does not fit).

@@ -941,6 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
     const int et = tid - 128 - grp * kEpiThreads, q = warp & 3;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const float neg_inf = __int_as_float(0xff800000u);
+    const float inv_rows = 1.0f / (float)R;  // mean pooling
     long long g = 0;
     bool ok = true;
     const int bt = tid - 128;  // 0..255 over both groups, for the row build
@@ -961,8 +962,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
             // pass 1: this thread owns observation row et (and a row of the second M tile)
             for (int mt = 0; mt < lay.mtiles; ++mt) {
               const int row = mt ? lay.Rp16 - 128 + et : et;
-              if (mt && row < 128) continue;  // the second tile overlaps the first on these lanes
-              const int bound = lim[row] - kt * kTileKeys;  // keys [0, bound) are visible
+              // The second M tile overlaps the first on rows below 128. tcgen05.ld
+              // is warp-collective (.sync.aligned), so only whole warps may skip
+              // it; lanes holding a duplicate row load and discard (bound 0
+              // masks every key, which leaves their running max and sum as is).
+              const bool dup = mt && row < 128;
+              if (__all_sync(kFull, dup)) continue;
+              const int bound = dup ? 0 : lim[row] - kt * kTileKeys;  // keys [0, bound) are visible
 #pragma unroll
               for (int h = 0; h < 4; h += 2) {
                 float v[64];
@@ -1002,39 +1008,74 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
             // pass 2: this thread owns key j of the tile; columns are observation rows
             const int j = kt * kTileKeys + et;
             const bool masked_tile = (kt + 1) * kTileKeys > L - P.nr + 1;
-            float m0 = neg_inf, m1 = neg_inf, m2 = neg_inf, m3 = neg_inf;
-            for (int c = 0; c < lay.Rp16; c += 64) {
-              float v[64];
-              tmem_ld32(col0 + (uint32_t)c, *reinterpret_cast<float(*)[32]>(&v[0]));
-              tmem_ld32(col0 + (uint32_t)c + 32, *reinterpret_cast<float(*)[32]>(&v[32]));  // inside the buffer
-              tmem_wait_ld();
-              if (!masked_tile && c + 64 <= R) {
+            if (P.pool_mean) {
+              // mean pooling: the weights exp2(l - lse) summed over the rows
+              // (inaccessible and padding rows add 0), divided by R
+              float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+              for (int c = 0; c < lay.Rp16; c += 64) {
+                float v[64];
+                tmem_ld32(col0 + (uint32_t)c, *reinterpret_cast<float(*)[32]>(&v[0]));
+                tmem_ld32(col0 + (uint32_t)c + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+                tmem_wait_ld();
                 const float4* l4 = reinterpret_cast<const float4*>(lse + c);
+                if (!masked_tile && c + 64 <= R) {
 #pragma unroll
-                for (int e = 0; e < 64; e += 4) {
-                  const float4 l = l4[e >> 2];
-                  m0 = fmaxf(m0, v[e] - l.x);
-                  m1 = fmaxf(m1, v[e + 1] - l.y);
-                  m2 = fmaxf(m2, v[e + 2] - l.z);
-                  m3 = fmaxf(m3, v[e + 3] - l.w);
-                }
-              } else {
-                // rows r >= R carry lim = 0, so the visibility test masks them too
-                const float4* l4 = reinterpret_cast<const float4*>(lse + c);
-                const int4* b4 = reinterpret_cast<const int4*>(lim + c);
+                  for (int e = 0; e < 64; e += 4) {
+                    const float4 l = l4[e >> 2];
+                    a0 += fast_exp2(v[e] - l.x);
+                    a1 += fast_exp2(v[e + 1] - l.y);
+                    a2 += fast_exp2(v[e + 2] - l.z);
+                    a3 += fast_exp2(v[e + 3] - l.w);
+                  }
+                } else {
+                  const int4* b4 = reinterpret_cast<const int4*>(lim + c);
 #pragma unroll
-                for (int e = 0; e < 64; e += 4) {
-                  const float4 l = l4[e >> 2];
-                  const int4 bd = b4[e >> 2];
-                  m0 = fmaxf(m0, j < bd.x ? v[e] - l.x : neg_inf);
-                  m1 = fmaxf(m1, j < bd.y ? v[e + 1] - l.y : neg_inf);
-                  m2 = fmaxf(m2, j < bd.z ? v[e + 2] - l.z : neg_inf);
-                  m3 = fmaxf(m3, j < bd.w ? v[e + 3] - l.w : neg_inf);
+                  for (int e = 0; e < 64; e += 4) {
+                    const float4 l = l4[e >> 2];
+                    const int4 bd = b4[e >> 2];
+                    a0 += j < bd.x ? fast_exp2(v[e] - l.x) : 0.f;
+                    a1 += j < bd.y ? fast_exp2(v[e + 1] - l.y) : 0.f;
+                    a2 += j < bd.z ? fast_exp2(v[e + 2] - l.z) : 0.f;
+                    a3 += j < bd.w ? fast_exp2(v[e + 3] - l.w) : 0.f;
+                  }
                 }
               }
+              if (j < L) s_u[j] = ((a0 + a1) + (a2 + a3)) * inv_rows;
+            } else {
+              float m0 = neg_inf, m1 = neg_inf, m2 = neg_inf, m3 = neg_inf;
+              for (int c = 0; c < lay.Rp16; c += 64) {
+                float v[64];
+                tmem_ld32(col0 + (uint32_t)c, *reinterpret_cast<float(*)[32]>(&v[0]));
+                tmem_ld32(col0 + (uint32_t)c + 32, *reinterpret_cast<float(*)[32]>(&v[32]));  // inside the buffer
+                tmem_wait_ld();
+                if (!masked_tile && c + 64 <= R) {
+                  const float4* l4 = reinterpret_cast<const float4*>(lse + c);
+  #pragma unroll
+                  for (int e = 0; e < 64; e += 4) {
+                    const float4 l = l4[e >> 2];
+                    m0 = fmaxf(m0, v[e] - l.x);
+                    m1 = fmaxf(m1, v[e + 1] - l.y);
+                    m2 = fmaxf(m2, v[e + 2] - l.z);
+                    m3 = fmaxf(m3, v[e + 3] - l.w);
+                  }
+                } else {
+                  // rows r >= R carry lim = 0, so the visibility test masks them too
+                  const float4* l4 = reinterpret_cast<const float4*>(lse + c);
+                  const int4* b4 = reinterpret_cast<const int4*>(lim + c);
+  #pragma unroll
+                  for (int e = 0; e < 64; e += 4) {
+                    const float4 l = l4[e >> 2];
+                    const int4 bd = b4[e >> 2];
+                    m0 = fmaxf(m0, j < bd.x ? v[e] - l.x : neg_inf);
+                    m1 = fmaxf(m1, j < bd.y ? v[e + 1] - l.y : neg_inf);
+                    m2 = fmaxf(m2, j < bd.z ? v[e + 2] - l.z : neg_inf);
+                    m3 = fmaxf(m3, j < bd.w ? v[e + 3] - l.w : neg_inf);
+                  }
+                }
+              }
+              const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+              if (j < L) s_u[j] = mx == neg_inf ? 0.f : fast_exp2(mx);
             }
-            const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-            if (j < L) s_u[j] = mx == neg_inf ? 0.f : fast_exp2(mx);
           }
           tc_fence_before();
           mbar_arrive(&tempty[b]);

@@ -86,3 +86,11 @@ for _b in (256, 512, 1024, 2048, 4096):
     WORKLOADS[f"r1_qwen7b_b128_k{_b}"] = Workload(
         name=f"r1_qwen7b_b128_k{_b}", layers=28, batch=128, heads=28, kv_heads=4, theta=1e4,
         budget=_b, centres=6, steps=32768, **_COMMON)
+
+# The pages' eviction schedule (BeaconKV reading notes §2.3): the cache grows to
+# B_max = 2048 and is cut to B_min = 7/8 B_max = 1792, so each eviction drops
+# 256 slots and 256 decode steps separate evictions (FPS still runs whenever
+# the beacon buffer fills, every 16 appends). Qwen3-4B head shape, batch 192.
+WORKLOADS["qwen3_4b_b192_sched78"] = WORKLOADS["qwen3_4b_b192"].with_(
+    name="qwen3_4b_b192_sched78", budget=1792, period=256)
+

@@ -66,7 +66,7 @@ def check_keep_set(gpu_kept, s_orc, orc_kept, L, prefix, recent, budget):
 
 def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "cpu",
                  steps: int | None = None, max_failures: int = 20,
-                 query_hook=None, order_free: bool = False) -> LockstepReport:
+                 query_hook=None, order_free: bool = False, pool: str = "max") -> LockstepReport:
     from kv_cache_eviction_head_gb300 import bkv
 
     dev = torch.device("cuda")
@@ -82,7 +82,8 @@ def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "c
                           fps_keep=w.fps_keep, layers=w.layers, batch=w.batch,
                           max_cache=w.max_cache, rope_theta=w.theta,
                           flags=bkv.BKV_FLAG_KEEP_SCORES
-                          | (bkv.BKV_FLAG_ORDER_FREE if order_free else 0))
+                          | (bkv.BKV_FLAG_ORDER_FREE if order_free else 0)
+                          | (bkv.BKV_FLAG_MEAN_POOL if pool == "mean" else 0))
     ws = torch.empty(bkv.bkv_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
     h = bkv.bkv_create(cfg, ws, torch.cuda.current_stream())
 
@@ -90,7 +91,7 @@ def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "c
         sample_units = [(l, b, kh) for l in range(w.layers) for b in range(w.batch)
                         for kh in range(w.kv_heads)]
     oracles = {u: UnitOracle(G, d, w.theta, w.budget, w.prefix, w.recent, w.fps_cap, w.fps_keep,
-                             order_free=order_free)
+                             order_free=order_free, pool=pool)
                for u in sample_units}
     live = set(sample_units)
     idx_dev = torch.device(gen_device)

@@ -51,6 +51,9 @@ def test_tiny_full_stream():
     ("ragged_budget", dict(budget=200, steps=300)),
     ("small_buffer", dict(fps_cap=6, fps_keep=2)),
     ("batch_layers", dict(layers=2, batch=3, heads=8, kv_heads=2, steps=200)),
+    # 5 heads x (12..31 beacons + 16 recents): observation rows sweep 140..235,
+    # so the second M tile starts at every 16-row offset past 128 (a split warp)
+    ("gqa5_rows_sweep", dict(heads=5, kv_heads=1, fps_keep=12, steps=400)),
 ])
 def test_tiny_variants(name, over):
     w = TINY.with_(**{"steps": 240, **over})
@@ -169,6 +172,61 @@ def test_order_free_needs_recent_window_inside_the_tail():
         bkv.bkv_sync(h)
     finally:
         bkv.bkv_destroy(h)
+
+
+# ---------------------------------------------------------------------------- the pages' variants
+
+@pytest.mark.parametrize("name,over", [
+    ("base", dict()),
+    ("gqa7", dict(heads=7, kv_heads=1)),
+    ("zero_beacons", dict(fps_cap=16, fps_keep=0)),
+    ("ragged_budget", dict(budget=200, steps=300)),
+])
+def test_mean_pool_tiny_variants(name, over):
+    """Mean pooling over queries and heads (Table 2's ablation) on whole tiny
+    streams: scores within tolerance, keep sets, compaction and FPS as ever."""
+    w = TINY.with_(**over)
+    rep = run_lockstep(w, seed=0xBEAC8 + len(name), pool="mean")
+    assert_clean(rep, min_evictions=3)
+
+
+def test_mean_pool_r1_qwen7b_b128_k1024_full_size_sampled_units():
+    """Mean pooling at full size on the shape Table 2 uses (R1-Distill-Qwen-7B)."""
+    w = WORKLOADS["r1_qwen7b_b128_k1024"]
+    units = [(0, 0, 0), (27, 127, 3), (13, 64, 1), (21, 7, 2)]
+    rep = run_lockstep(w, seed=0xBEAC9, sample_units=units, gen_device="cuda",
+                       steps=w.max_cache + 2 * w.period, pool="mean")
+    assert_clean(rep, min_evictions=3)
+
+
+@pytest.mark.parametrize("recent,beacons", [(4, 28), (1, 31), (31, 1)])
+def test_recent_beacon_splits(recent, beacons):
+    """Table 1's splits of the 32 observation queries per head: n_rq recent
+    queries and fps_keep beacons (4 + 28, 1 + 31, 31 + 1)."""
+    w = TINY.with_(fps_cap=32, fps_keep=beacons, steps=400)
+    assert w.fps_cap - w.fps_keep == recent
+    rep = run_lockstep(w, seed=0xBEACA + recent)
+    assert_clean(rep, min_evictions=10)
+
+
+def test_seven_eighths_schedule_tiny():
+    """The pages' schedule at tiny scale: B_max = 256 cut to 7/8 = 224, so 32
+    slots drop per eviction and 32 steps separate evictions."""
+    w = TINY.with_(budget=224, period=32, steps=600)
+    rep = run_lockstep(w, seed=0xBEACB)
+    assert_clean(rep, min_evictions=8)
+
+
+def test_seven_eighths_schedule_qwen3_4b_b192_full_size_sampled_units():
+    """B_max = 2048 cut to 1792 at full size: 256 drops per unit and eviction,
+    FPS every 16 appends between evictions, in slot order and order-free."""
+    w = WORKLOADS["qwen3_4b_b192_sched78"]
+    units = [(0, 0, 0), (35, 191, 7), (17, 100, 5), (8, 1, 1)]
+    for order_free in (False, True):
+        rep = run_lockstep(w, seed=0xBEACC, sample_units=units, gen_device="cuda",
+                           steps=w.max_cache + w.period, order_free=order_free)
+        assert_clean(rep, min_evictions=2)
+        assert rep.units_checked == len(units) * rep.evictions
 
 
 def wide_queries(t, q):
