@@ -356,7 +356,8 @@ def run_ours(args, w):
                          "alg_bytes_per_launch": kb[name],
                          "gbs": gbs, "frac": (gbs / peak) if gbs else None}
     dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches_per_step"])
-    traffic = read_traffic(dom, w.name)
+    traffic_key = w.name + ("+order-free" if args.order_free else "") + ("+mean" if args.pool == "mean" else "")
+    traffic = read_traffic(dom, traffic_key)
     roofline = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak,
                 "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": traffic,
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
