@@ -277,14 +277,80 @@ __device__ __forceinline__ void merge8(u64 (&list)[8], const u64 (&k)[8]) {
       if ((i & dd) == 0) cswap(list[i], list[i + dd]);
 }
 
-__device__ bool select_keep(const float* sc, int L, int prefix, int recent, int budget, int32_t* out,
-                            uint32_t* dropped, int* drops, bool order_free) {
-  static_assert(kList == 8, "the list networks are written for 8 keys");
+// Large drop counts (D > kRadixFrom): the D-th smallest score is found digit
+// by digit (four 8-bit radix passes over a 256-bin shared histogram of the
+// candidates that match the digits chosen so far); every candidate below it
+// is dropped, and among those equal to it the highest slots fill the rest.
+constexpr int kRadixFrom = 32;
+__device__ bool radix_drop(const float* sc, int c0, int c1, int D, uint32_t* dropped, int* hist) {
   const int lane = threadIdx.x & 31;
-  const int c0 = prefix < L ? prefix : L;
-  const int c1 = L - recent > c0 ? L - recent : c0;
-  const int D = L - budget;
-  for (int wd = lane; wd < (L + 31) / 32; wd += 32) dropped[wd] = 0u;
+  bool bad = false;
+  for (int j = c0 + lane; j < c1; j += 32) bad |= sc[j] != sc[j];
+  uint32_t prefix = 0u, mask = 0u;
+  int rank = D;  // rank (1-based) of the threshold among candidates matching `prefix`
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = lane; i < 256; i += 32) hist[i] = 0;
+    __syncwarp();
+    for (int j = c0 + lane; j < c1; j += 32) {
+      const uint32_t bits = __float_as_uint(sc[j]);
+      if ((bits & mask) == prefix) atomicAdd(&hist[(bits >> shift) & 0xFFu], 1);
+    }
+    __syncwarp();
+    // lane l owns bins [8l, 8l + 8): the digit where the running count reaches rank
+    int cnt[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      cnt[i] = hist[8 * lane + i];
+      sum += cnt[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const int excl = incl - sum;
+    const unsigned owner = __ballot_sync(kFull, excl < rank && rank <= incl);
+    const int src = __ffs(owner) - 1;
+    int digit = 0, below = 0;
+    if (lane == src) {
+      int run = excl;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (run + cnt[i] >= rank) {
+          digit = 8 * lane + i;
+          below = run;
+          break;
+        }
+        run += cnt[i];
+      }
+    }
+    digit = __shfl_sync(kFull, digit, src);
+    below = __shfl_sync(kFull, below, src);
+    rank -= below;
+    prefix |= (uint32_t)digit << shift;
+    mask |= 0xFFu << shift;
+    __syncwarp();
+  }
+  // drop every candidate below the threshold, then `rank` of those equal to it,
+  // highest slots first
+  for (int j = c0 + lane; j < c1; j += 32)
+    if (__float_as_uint(sc[j]) < prefix) atomicOr(&dropped[j >> 5], 1u << (j & 31));
+  int need = rank;
+  for (int top = c1 - 1; top >= c0 && need > 0; top -= 32) {
+    const int j = top - lane;  // lane 0 takes the highest slot of the chunk
+    const bool tie = j >= c0 && __float_as_uint(sc[j]) == prefix;
+    const unsigned tb = __ballot_sync(kFull, tie);
+    const int before = __popc(tb & ((1u << lane) - 1u));  // ties at higher slots in this chunk
+    if (tie && before < need) atomicOr(&dropped[j >> 5], 1u << (j & 31));
+    need -= __popc(tb);
+  }
+  return __any_sync(kFull, bad);
+}
+
+// Small drop counts: each lane's kList smallest keys, then D warp minima.
+__device__ bool list_drop(const float* sc, int c0, int c1, int D, uint32_t* dropped) {
+  const int lane = threadIdx.x & 31;
   u64 list[kList];
   bool bad = false;
   // the lane's kList smallest keys above `after`
@@ -330,6 +396,19 @@ __device__ bool select_keep(const float* sc, int L, int prefix, int recent, int 
       }
     }
   }
+  return __any_sync(kFull, bad);
+}
+
+__device__ bool select_keep(const float* sc, int L, int prefix, int recent, int budget, int32_t* out,
+                            uint32_t* dropped, int* drops, bool order_free, int* hist) {
+  static_assert(kList == 8, "the list networks are written for 8 keys");
+  const int lane = threadIdx.x & 31;
+  const int c0 = prefix < L ? prefix : L;
+  const int c1 = L - recent > c0 ? L - recent : c0;
+  const int D = L - budget;
+  for (int wd = lane; wd < (L + 31) / 32; wd += 32) dropped[wd] = 0u;
+  __syncwarp();
+  const bool bad = D > kRadixFrom ? radix_drop(sc, c0, c1, D, dropped, hist) : list_drop(sc, c0, c1, D, dropped);
   __syncwarp();
   // dropped slots ascending: per-word counts, a warp prefix sum, then the bits
   const int words = (L + 31) / 32;
@@ -372,9 +451,13 @@ __device__ bool select_keep(const float* sc, int L, int prefix, int recent, int 
       out[drops[k]] = x;
     }
   }
-  return __any_sync(kFull, bad);
+  return bad;
 }
 
+// Miscellaneous shared memory: control word [0, 64), dropped-slot bitmask
+// [64, 1088) (L <= 8192), copier chunk descriptors [1536, 1664), order-free
+// pairs [1664, 1920), radix histogram of the selector [2048, 3072).
+constexpr int kMiscBytes = 3072;
 constexpr int kChunkRows = 32;                   // rows per compaction chunk
 constexpr int kChunkBytes = kChunkRows * kD * 2;  // 8 KB
 constexpr int kPfRows = 512;                      // L2 prefetch lead of the copier (few chunk buffers only)
@@ -406,7 +489,7 @@ __host__ __device__ inline Layout make_layout(int R, int L, int nr, int budget, 
   s.D = L - budget;
   const size_t qbytes = ((size_t)s.qrows * 256 + 1023) / 1024 * 1024;  // two 128-byte slabs per row
   const size_t small = (size_t)s.rows64 * 8 + (size_t)s.qrows * 16 + (size_t)s.qrows * 8 +
-                       2 * (size_t)s.D * 4 + 16 + 64 * 8 + 2048 + 64;
+                       2 * (size_t)s.D * 4 + 16 + 64 * 8 + kMiscBytes + 64;
   const size_t cap = 227 * 1024 - 1024;  // 1 KB kept for aligning the dynamic base
   const size_t scb = (size_t)s.Lp * 4;
   static const int plans[][3] = {{4, 0, 2}, {3, 0, 2}, {2, 0, 2}, {2, 0, 1}};          // no compaction
@@ -449,7 +532,7 @@ __host__ __device__ inline Layout make_layout(int R, int L, int nr, int budget, 
   s.bars = (off + 7) & ~(size_t)7;
   off = s.bars + 64 * 8;
   s.misc = off;
-  off += 2048;
+  off += kMiscBytes;
   s.total = off + 1024;
   return s;
 }
@@ -922,7 +1005,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       const int u = blockIdx.x + it * gridDim.x;
       const float* s_u = sc + (size_t)b * lay.Lp;
       const bool bad = select_keep(s_u, L, P.prefix, P.recent, P.budget, P.kept + (size_t)u * P.budget,
-                                   dropbits, dlist + db * lay.D, P.compact == 2);
+                                   dropbits, dlist + db * lay.D, P.compact == 2,
+                                   reinterpret_cast<int*>(smem + lay.misc + 2048));
       if (bad && lane == 0) latch(P.status, BKV_ERR_NONFINITE);
       if (P.scores) {
         float* so = P.scores + (size_t)u * P.max_cache;

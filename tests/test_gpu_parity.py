@@ -217,6 +217,16 @@ def test_seven_eighths_schedule_tiny():
     assert_clean(rep, min_evictions=8)
 
 
+@pytest.mark.parametrize("period", [48, 64])
+def test_large_drop_counts_tiny(period):
+    """More than 32 drops per eviction take the selector's radix path."""
+    w = TINY.with_(budget=160, period=period, steps=520)
+    rep = run_lockstep(w, seed=0xBEACD + period)
+    assert_clean(rep, min_evictions=5)
+    rep = run_lockstep(w, seed=0xBEACD + period, order_free=True)
+    assert_clean(rep, min_evictions=5)
+
+
 def test_seven_eighths_schedule_qwen3_4b_b192_full_size_sampled_units():
     """B_max = 2048 cut to 1792 at full size: 256 drops per unit and eviction,
     FPS every 16 appends between evictions, in slot order and order-free."""
