@@ -21,6 +21,7 @@ from .beaconkv import (
     exact_dot,
     gram_exact,
     cosine_matrix,
+    coverage,
     fps,
     attention_weights,
     max_pool,
@@ -31,6 +32,6 @@ from .beaconkv import (
 )
 
 __all__ = [
-    "bf16_to_f64", "rope", "exact_dot", "gram_exact", "cosine_matrix", "fps",
+    "bf16_to_f64", "rope", "exact_dot", "gram_exact", "cosine_matrix", "coverage", "fps",
     "attention_weights", "max_pool", "mean_pool", "select_keep", "order_free_layout", "UnitOracle",
 ]

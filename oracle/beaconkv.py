@@ -190,6 +190,25 @@ def mean_pool(W) -> np.ndarray:
     return W.sum(axis=0) / W.shape[0]
 
 
+def coverage(obs, future) -> list[float]:
+    """Future-query coverage (BeaconKV reading notes §3.2, Figure 6): for each
+    future query, the largest cosine between it and any row of the observation
+    set, with the cosine of cosine_matrix (exact dot products, IEEE float64).
+    -inf for an empty observation set."""
+    obs = [bf16_to_f64(o) for o in obs]
+    out = []
+    for q in future:
+        qv = bf16_to_f64(q)
+        gqq = exact_dot(qv, qv)
+        best = -math.inf
+        for o in obs:
+            goo = exact_dot(o, o)
+            c = 0.0 if gqq == 0.0 or goo == 0.0 else exact_dot(qv, o) / math.sqrt(gqq * goo)
+            best = max(best, c)
+        out.append(best)
+    return out
+
+
 # ----------------------------------------------------------------------------
 # keep set and compaction (BeaconKV reading notes, §2.3 eq. 8)
 
@@ -350,6 +369,12 @@ class UnitOracle:
             st.rq.clear()
             traces.append(list(st.trace))
         return EvictResult(kept=kept, score=score, obs_rows=nobs, traces=traces, layout=layout)
+
+    def coverage(self, future_q) -> list[list[float]]:
+        """Per query head, coverage() of its current observation set (beacons,
+        then recents: what the next eviction scores) over future_q[h] rows."""
+        return [coverage(list(st.bq) + [q for q, _ in st.rq], future_q[h])
+                for h, st in enumerate(self.heads)]
 
     # -- state injection (steady-state samples for timing) -------------------
     def load_state(self, bq_rows, rq_rows, rq_pos, K, V, pos) -> None:

@@ -17,7 +17,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import (UnitOracle, attention_weights, bf16_to_f64, cosine_matrix, exact_dot, fps,
+from oracle import (UnitOracle, attention_weights, bf16_to_f64, cosine_matrix, coverage, exact_dot, fps,
                     gram_exact, max_pool, mean_pool, order_free_layout, rope, select_keep)
 from synth import kv_bytes_per_token, to_bits
 
@@ -369,6 +369,43 @@ def test_mean_pool_scores_sum_to_one_and_bound_the_max(seed):
     assert math.isclose(float(mp.sum()), 1.0, rel_tol=1e-12)
     assert np.all(mp <= max_pool(W) + 1e-15)
     assert np.allclose(mean_pool(W[:1]), max_pool(W[:1]), rtol=0, atol=0)
+
+
+def test_coverage_closed_forms():
+    """A member of the set covers itself (cosine 1 up to the float64 square
+    root), its negation scores -1, an orthogonal query 0, a zero query 0, a
+    scaled copy 1; the max is over the whole set; an empty set gives -inf."""
+    e = np.eye(128)[:3]
+    obs = [bf16_bits(e[0]), bf16_bits(e[1] * 2.0)]
+    fut = [bf16_bits(e[0]), bf16_bits(-e[0]), bf16_bits(e[2]), bf16_bits(np.zeros(128)),
+           bf16_bits(e[1] * 0.5), bf16_bits(e[0] + e[1])]
+    got = coverage(obs, fut)
+    assert got[0] == 1.0 and got[1] == 0.0 and got[2] == 0.0 and got[3] == 0.0
+    assert got[4] == 1.0
+    assert math.isclose(got[5], 1 / math.sqrt(2), rel_tol=1e-15)
+    assert coverage([bf16_bits(-e[0])], [bf16_bits(e[0])]) == [-1.0]
+    assert coverage([], [bf16_bits(e[0])]) == [-math.inf]
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_coverage_matches_rational_brute_force(seed):
+    """Against exact rational arithmetic: the max cosine is attained by the
+    row with the largest G_qo / sqrt(G_oo), and its float64 value is the
+    correctly rounded quotient of the exact dot products."""
+    obs = rand_bits((7, 128), seed=200 + seed)
+    fut = rand_bits((5, 128), seed=300 + seed)
+    got = coverage(obs, fut)
+    for f, c in zip(fut, got):
+        fq = [Fraction(float(v)) for v in bf16_to_f64(f)]
+        gqq = sum(x * x for x in fq)
+        best = None
+        for o in obs:
+            ov = [Fraction(float(v)) for v in bf16_to_f64(o)]
+            goo = sum(x * x for x in ov)
+            gqo = sum(x * y for x, y in zip(fq, ov))
+            val = float(gqo) / math.sqrt(float(gqq) * float(goo))
+            best = val if best is None else max(best, val)
+        assert c == best
 
 
 # ---------------------------------------------------------------------------- keep set
