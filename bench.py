@@ -364,6 +364,29 @@ def run_ours(args, w):
                 else "fallback 6.8 TB/s"}
     pbytes = path_bytes(w, R, rows_moved, heads_total)
 
+    # ---- future-query coverage of the observation sets (diagnostic, untimed step)
+    coverage = None
+    if args.coverage > 0:
+        g = torch.Generator(device=dev).manual_seed(99)
+        qf = torch.randn(args.coverage, w.layers, w.batch, w.heads, w.d, generator=g,
+                         device=dev).to(torch.bfloat16)
+        cov = torch.empty(w.layers, w.batch, w.heads, args.coverage, dtype=torch.float64, device=dev)
+        for _ in range(2):
+            bkv.bkv_coverage(h, qf, cov)
+        bkv.bkv_profile(h, True)
+        ca, cb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ca.record(cs)
+        for _ in range(3):
+            bkv.bkv_coverage(h, qf, cov)
+        cb.record(cs)
+        torch.cuda.synchronize(dev)
+        bkv.bkv_profile(h, False)
+        ms = ca.elapsed_time(cb) / 3
+        st = bkv.bkv_get_stats(h)
+        pairs = heads_total * (st.beacons + st.recents) * args.coverage
+        coverage = {"n_future": args.coverage, "obs_rows_per_head": st.beacons + st.recents,
+                    "ms_per_launch": ms, "exact_cosines_per_s": pairs / (ms / 1e3)}
+
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
@@ -421,6 +444,7 @@ def run_ours(args, w):
                      "rows_moved_per_unit": rows_moved / w.units, "obs_rows_per_unit": R},
             "kernels": kernels,
             "clocks": clocks,
+            "coverage": coverage,
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
@@ -513,6 +537,8 @@ def main():
                     help="aggregation of the attention weights over observation rows")
     ap.add_argument("--fps-keep", type=int, default=None,
                     help="beacons kept per head (recent queries = 32 - this), Table 1's splits")
+    ap.add_argument("--coverage", type=int, default=0,
+                    help="also time bkv_coverage over this many future queries (diagnostic)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()

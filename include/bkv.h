@@ -157,6 +157,19 @@ bkv_status bkv_append_queries(bkv_handle h, const void* q_pre, int64_t step);
 bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache_len,
                      int64_t step, int32_t* kept);
 
+/* Future-query coverage (notes §3.2, Figure 6): for every query head and each
+ * of n_future pre-RoPE queries, the largest cosine between that query and the
+ * head's current observation set - its beacons and recent queries, the rows
+ * the next bkv_evict would score. Call it before bkv_evict (which replaces
+ * the set) with the queries of the steps that follow. The cosine is the FPS
+ * arithmetic: exact dot products rounded once to fp64, IEEE fp64 division and
+ * square root, 0 for a zero vector; -inf where a head's set is empty.
+ *   q_future: device bf16 [n_future][layers][batch][heads][d], 16-B aligned.
+ *   out:      device double [layers][batch][heads][n_future], 8-B aligned.
+ * Asynchronous on the handle's stream; BKV_ERR_INVALID_ARG for null or
+ * misaligned pointers or n_future < 1. */
+bkv_status bkv_coverage(bkv_handle h, const void* q_future, int32_t n_future, double* out);
+
 /* Waits for the handle's stream, then returns and clears the latched device
  * status (BKV_OK when no device error was seen), or BKV_ERR_CUDA. */
 bkv_status bkv_sync(bkv_handle h);
@@ -183,7 +196,7 @@ bkv_status bkv_get_head_state(bkv_handle h, int32_t layer, int32_t seq, int32_t 
 /* Per-kernel device time, from CUDA events the library records on its stream
  * around each of its launches while profiling is on. Index with BKV_K_*. */
 enum { BKV_K_APPEND = 0, BKV_K_ROPE = 1, BKV_K_SCORE = 2 /* score, keep set and compaction */,
-       BKV_K_FPS = 3, BKV_K_COUNT = 4 };
+       BKV_K_FPS = 3, BKV_K_COVERAGE = 4, BKV_K_COUNT = 5 };
 typedef struct bkv_kernel_times {
   double ms[BKV_K_COUNT];          /* summed launch durations, milliseconds */
   uint64_t launches[BKV_K_COUNT];  /* launches summed */

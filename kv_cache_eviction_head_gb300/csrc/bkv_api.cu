@@ -308,6 +308,26 @@ bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache
   return BKV_OK;
 }
 
+bkv_status bkv_coverage(bkv_handle h, const void* q_future, int32_t n_future, double* out) {
+  if (!h || !q_future || !out || n_future < 1 || !aligned(q_future, 16) || !aligned(out, 8))
+    return BKV_ERR_INVALID_ARG;
+  bkv::CoverageParams p{};
+  p.bq = h->bq();
+  p.rq = h->rq();
+  p.q_future = static_cast<const uint4*>(q_future);
+  p.out = out;
+  p.heads_total = h->heads_total;
+  p.fps_cap = h->cfg.fps_cap;
+  p.n_rq = h->n_rq;
+  p.nb = h->nb;
+  p.nr = h->nr;
+  p.ring_first = h->nr > 0 ? h->ring_slot(h->last_step - h->nr + 1) : 0;
+  p.n_future = n_future;
+  if (h->timed(BKV_K_COVERAGE, [&] { return bkv::launch_coverage(p, h->stream); }) != cudaSuccess)
+    return BKV_ERR_CUDA;
+  return BKV_OK;
+}
+
 bkv_status bkv_sync(bkv_handle h) {
   if (!h) return BKV_ERR_INVALID_ARG;
   uint32_t code = 0;

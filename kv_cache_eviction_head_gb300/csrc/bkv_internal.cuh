@@ -61,6 +61,18 @@ struct FpsParams {
 cudaError_t launch_fps(const FpsParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
+// future-query coverage of each head's observation set (diagnostic)
+struct CoverageParams {
+  const uint4* bq;        // [heads_total][fps_cap][d]; rows [0, nb) are beacons
+  const uint4* rq;        // [heads_total][n_rq][d]; nr recents from ring_first
+  const uint4* q_future;  // [n_future][heads_total][d]
+  double* out;            // [heads_total][n_future]
+  int64_t heads_total;
+  int fps_cap, n_rq, nb, nr, ring_first, n_future;
+};
+cudaError_t launch_coverage(const CoverageParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
 // score + keep-set selection: persistent CTAs over the units
 struct ScoreParams {
   CUtensorMap kmap[kMaxLayers];  // per layer: K as 2-D [batch*kv_heads*max_cache][d] bf16

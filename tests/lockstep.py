@@ -15,7 +15,9 @@ Agreement rules (per unit and eviction):
     the tie band does not make later rounds diverge);
   * order-free compaction (order_free=True): the returned layout is exactly the
     oracle's order_free_layout of the returned set, and K/V follow it;
-  * FPS traces after the eviction: identical pick order for every query head.
+  * FPS traces after the eviction: identical pick order for every query head;
+  * with coverage_n > 0, before each eviction: bkv_coverage over coverage_n
+    seeded future queries equals the oracle's coverage bit for bit (float64).
 """
 
 from __future__ import annotations
@@ -40,6 +42,7 @@ class LockstepReport:
     fps_heads_checked: int = 0
     max_score_rel: float = 0.0
     rows_moved: int = 0
+    coverage_checked: int = 0      # (head, future query) values compared
     failures: list = field(default_factory=list)
 
 
@@ -66,7 +69,8 @@ def check_keep_set(gpu_kept, s_orc, orc_kept, L, prefix, recent, budget):
 
 def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "cpu",
                  steps: int | None = None, max_failures: int = 20,
-                 query_hook=None, order_free: bool = False, pool: str = "max") -> LockstepReport:
+                 query_hook=None, order_free: bool = False, pool: str = "max",
+                 coverage_n: int = 0) -> LockstepReport:
     from kv_cache_eviction_head_gb300 import bkv
 
     dev = torch.device("cuda")
@@ -144,6 +148,29 @@ def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "c
                         live.discard((l, b, kh))
                         break
 
+            if coverage_n > 0:
+                g = torch.Generator().manual_seed(seed * 7919 + t)
+                qf = (torch.randn(coverage_n, w.layers, w.batch, w.heads, d, generator=g)
+                      * torch.exp2(torch.randint(-3, 4, (coverage_n, 1, 1, w.heads, 1), generator=g).float())
+                      ).to(torch.bfloat16)
+                if query_hook is not None:
+                    qf = torch.stack([query_hook(t + 1 + i, qf[i]) for i in range(coverage_n)])
+                cov = torch.empty(w.layers, w.batch, w.heads, coverage_n, dtype=torch.float64, device=dev)
+                bkv.bkv_coverage(h, qf.to(dev), cov)
+                cov_h = cov.cpu().numpy()
+                qf_bits = to_bits(qf)
+                for (l, b, kh) in sorted(live):
+                    want = oracles[(l, b, kh)].coverage(
+                        [qf_bits[:, l, b, kh * G + hg] for hg in range(G)])
+                    for hg in range(G):
+                        got = cov_h[l, b, kh * G + hg].tolist()
+                        rep.coverage_checked += coverage_n
+                        if got != want[hg]:
+                            i = next(i for i in range(coverage_n) if got[i] != want[hg][i])
+                            fail(f"t={t} unit {(l, b, kh)} head {hg}: coverage[{i}] "
+                                 f"gpu {got[i]!r} orc {want[hg][i]!r}")
+                            live.discard((l, b, kh))
+                            break
             bkv.bkv_evict(h, K, V, cache_len, t, kept)
             bkv.bkv_sync(h)
             rep.evictions += 1

@@ -239,6 +239,37 @@ def test_seven_eighths_schedule_qwen3_4b_b192_full_size_sampled_units():
         assert rep.units_checked == len(units) * rep.evictions
 
 
+# ---------------------------------------------------------------------------- coverage diagnostic
+
+def test_coverage_tiny_stream():
+    """bkv_coverage before every eviction of a whole tiny stream, 40 future
+    queries per head (two warps' worth), bit-exact against the oracle."""
+    rep = run_lockstep(TINY, seed=0xBEACE, coverage_n=40)
+    assert_clean(rep, min_evictions=24)
+    assert rep.coverage_checked == 4 * 40 * rep.evictions
+
+
+def test_coverage_wide_exponents_and_splits():
+    """Coverage through the wide-exponent path (future and observation rows
+    spanning far more than 20 binades, zero rows, duplicates) and with up to
+    62 observation rows per head (31 recents)."""
+    w = TINY.with_(steps=300)
+    rep = run_lockstep(w, seed=0xBEACF, query_hook=wide_queries, coverage_n=16)
+    assert_clean(rep, min_evictions=5)
+    w2 = TINY.with_(fps_cap=32, fps_keep=1, steps=300)
+    rep = run_lockstep(w2, seed=0xBEAD0, coverage_n=8)
+    assert_clean(rep, min_evictions=5)
+
+
+def test_coverage_qwen3_4b_b192_full_size_sampled_units():
+    w = WORKLOADS["qwen3_4b_b192"]
+    units = [(0, 0, 0), (35, 191, 7), (17, 100, 5)]
+    rep = run_lockstep(w, seed=0xBEAD1, sample_units=units, gen_device="cuda",
+                       steps=w.max_cache + w.period, coverage_n=8)
+    assert_clean(rep, min_evictions=2)
+    assert rep.coverage_checked == len(units) * w.group * 8 * rep.evictions
+
+
 def wide_queries(t, q):
     """Replaces some queries by vectors whose exponents span far more than 20
     binades (FPS's wide exact-sum path), by zero rows and by exact duplicates."""
