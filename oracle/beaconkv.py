@@ -370,6 +370,27 @@ class UnitOracle:
             traces.append(list(st.trace))
         return EvictResult(kept=kept, score=score, obs_rows=nobs, traces=traces, layout=layout)
 
+    def prefill(self, q_prompt, first_step: int) -> None:
+        """Initial observation state from a prompt (BeaconKV reading notes §2.2:
+        at prefill the first representatives are sampled from the input
+        queries). Per head, of the P prompt queries (positions first_step ...
+        first_step + P - 1), the last min(n_rq, P) become the recent queries at
+        their own positions, and the beacons are FPS(the earlier ones, fps_keep),
+        all of them when there are no more than fps_keep; the picks are the
+        head's trace. The prompt's keys and values go through append_kv."""
+        assert all(not st.bq and not st.rq for st in self.heads), "prefill needs a fresh state"
+        P = len(q_prompt[0])
+        nr = min(self.n_rq, P)
+        for h, st in enumerate(self.heads):
+            rows = [np.asarray(r, dtype=np.uint16).copy() for r in q_prompt[h]]
+            older = rows[:P - nr]
+            if older:
+                st.trace, keep = fps(bf16_to_f64(np.stack(older)), self.fps_keep)
+                st.bq = [older[i] for i in keep]
+            else:
+                st.trace = []
+            st.rq = deque((rows[P - nr + k], first_step + P - nr + k) for k in range(nr))
+
     def coverage(self, future_q) -> list[list[float]]:
         """Per query head, coverage() of its current observation set (beacons,
         then recents: what the next eviction scores) over future_q[h] rows."""

@@ -408,6 +408,40 @@ def test_coverage_matches_rational_brute_force(seed):
         assert c == best
 
 
+@pytest.mark.parametrize("P", [1, 3, 4, 6, 8])
+def test_prefill_of_a_short_prompt_equals_streaming_appends(P):
+    """While the earlier prompt queries fit in fps_keep no FPS runs either
+    way, so prefill must leave exactly the state of P single-step appends
+    (beacons = the spilled queries in order, recents = the last n_rq)."""
+    mk = lambda: UnitOracle(group=3, d=128, theta=1e6, budget=20, prefix=2, recent=4,
+                            fps_cap=8, fps_keep=4)
+    a, b = mk(), mk()
+    q = rand_bits((P, 3, 128), seed=400 + P)   # n_rq = 4, so at most fps_keep = 4 older queries
+    for t in range(P):
+        a.append_queries(q[t], 100 + t)
+    b.prefill([q[:, h] for h in range(3)], 100)
+    for sa, sb in zip(a.heads, b.heads):
+        assert [r.tobytes() for r in sa.bq] == [r.tobytes() for r in sb.bq]
+        assert [(r.tobytes(), p) for r, p in sa.rq] == [(r.tobytes(), p) for r, p in sb.rq]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_prefill_beacons_are_brute_force_fps_of_the_older_queries(seed):
+    """The beacons and trace are the greedy rule re-derived by brute force
+    (max-cosine-to-set recomputed from rational Gram entries) over the
+    prompt's queries older than the recent window."""
+    g = np.random.default_rng(seed)
+    P, n_rq, keep = int(g.integers(20, 36)), 5, 6
+    u = UnitOracle(group=1, d=128, theta=1e6, budget=20, prefix=2, recent=4, fps_cap=keep + n_rq,
+                   fps_keep=keep)
+    q = rand_bits((P, 128), seed=500 + seed)
+    u.prefill([q], 7)
+    want = fps_brute(q[:P - n_rq], keep)
+    assert u.heads[0].trace == want
+    assert [r.tobytes() for r in u.heads[0].bq] == [q[i].tobytes() for i in sorted(want)]
+    assert [p for _, p in u.heads[0].rq] == list(range(7 + P - n_rq, 7 + P))
+
+
 # ---------------------------------------------------------------------------- keep set
 
 @pytest.mark.parametrize("seed", range(20))
