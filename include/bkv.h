@@ -157,6 +157,28 @@ bkv_status bkv_append_queries(bkv_handle h, const void* q_pre, int64_t step);
 bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache_len,
                      int64_t step, int32_t* kept);
 
+/* Prefill (notes §2.2: at prefill the first representatives are sampled from
+ * the input queries). Sets every query head's observation state from the
+ * prompt's pre-RoPE queries: the last min(n_rq, P) become the recent queries
+ * at their own positions, and the beacons are FPS (Algorithm 1) of the earlier
+ * ones, fps_keep of them (all when fewer), in candidate order. The caller
+ * writes the prompt's keys and values to cache slots [0, P) itself; when
+ * P > budget, bkv_evict(K, V, P, first_step + P - 1, kept) then evicts the
+ * prompt down to the budget, and decoding continues with bkv_append_queries
+ * at step first_step + P.
+ *   q_prompt:   device bf16 [P][layers][batch][heads][d], 16-B aligned.
+ *   P:          1 <= P <= max_cache.
+ *   first_step: position of the first prompt token, >= 0.
+ *   trace_out:  optional device int32 [layers][batch][heads][min(fps_keep, N)]
+ *               receiving each head's picks (indices into its N = P - recents
+ *               older queries) in pick order; NULL to skip. The int8 trace of
+ *               bkv_get_fps_trace is not updated.
+ * Needs a handle with no queries appended yet (BKV_ERR_STATE otherwise);
+ * BKV_ERR_UNSUPPORTED if P - min(n_rq, P) exceeds what one CTA's shared
+ * memory holds (about 20K older queries). */
+bkv_status bkv_prefill(bkv_handle h, const void* q_prompt, int32_t P, int64_t first_step,
+                       int32_t* trace_out);
+
 /* Future-query coverage (notes §3.2, Figure 6): for every query head and each
  * of n_future pre-RoPE queries, the largest cosine between that query and the
  * head's current observation set - its beacons and recent queries, the rows
@@ -196,7 +218,7 @@ bkv_status bkv_get_head_state(bkv_handle h, int32_t layer, int32_t seq, int32_t 
 /* Per-kernel device time, from CUDA events the library records on its stream
  * around each of its launches while profiling is on. Index with BKV_K_*. */
 enum { BKV_K_APPEND = 0, BKV_K_ROPE = 1, BKV_K_SCORE = 2 /* score, keep set and compaction */,
-       BKV_K_FPS = 3, BKV_K_COVERAGE = 4, BKV_K_COUNT = 5 };
+       BKV_K_FPS = 3, BKV_K_COVERAGE = 4, BKV_K_PREFILL = 5, BKV_K_COUNT = 6 };
 typedef struct bkv_kernel_times {
   double ms[BKV_K_COUNT];          /* summed launch durations, milliseconds */
   uint64_t launches[BKV_K_COUNT];  /* launches summed */

@@ -34,10 +34,10 @@ BKV_FLAG_ORDER_FREE = 2
 BKV_FLAG_MEAN_POOL = 4
 
 EXPORTED = ["bkv_workspace_bytes", "bkv_create", "bkv_set_stream", "bkv_append_queries",
-            "bkv_evict", "bkv_coverage", "bkv_sync", "bkv_get_fps_trace", "bkv_get_scores", "bkv_get_head_state",
+            "bkv_evict", "bkv_prefill", "bkv_coverage", "bkv_sync", "bkv_get_fps_trace", "bkv_get_scores", "bkv_get_head_state",
             "bkv_profile", "bkv_profile_read", "bkv_score_select_noalloc", "bkv_get_stats",
             "bkv_destroy", "bkv_status_str"]
-KERNELS = ["append", "rope", "score_select", "fps", "coverage"]
+KERNELS = ["append", "rope", "score_select", "fps", "coverage", "prefill"]
 
 
 class BkvConfig(ctypes.Structure):
@@ -56,7 +56,7 @@ class BkvStats(ctypes.Structure):
 
 
 class BkvKernelTimes(ctypes.Structure):
-    _fields_ = [("ms", ctypes.c_double * 5), ("launches", ctypes.c_uint64 * 5)]
+    _fields_ = [("ms", ctypes.c_double * 6), ("launches", ctypes.c_uint64 * 6)]
 
 
 _vp, _sz, _i32, _i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64
@@ -66,6 +66,7 @@ _lib.bkv_set_stream.argtypes = [_vp, _vp]
 _lib.bkv_append_queries.argtypes = [_vp, _vp, _i64]
 _lib.bkv_evict.argtypes = [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _i64, _vp]
 _lib.bkv_coverage.argtypes = [_vp, _vp, _i32, _vp]
+_lib.bkv_prefill.argtypes = [_vp, _vp, _i32, _i64, _vp]
 _lib.bkv_sync.argtypes = [_vp]
 _lib.bkv_get_fps_trace.argtypes = [_vp, _vp, _sz]
 _lib.bkv_get_scores.argtypes = [_vp, _vp, _sz]
@@ -156,6 +157,14 @@ def bkv_evict_ptrs(h: Handle, kptrs, vptrs, cache_len: int, step: int, kept_ptr:
     """bkv_evict with raw device pointers (pre-marshalled pointer arrays allowed)."""
     _check(_lib.bkv_evict(_vp(h.ptr), kptrs, vptrs, _i32(cache_len), _i64(step), _vp(kept_ptr)),
            "bkv_evict")
+
+
+def bkv_prefill(h: Handle, q_prompt, first_step: int, trace_out=None) -> None:
+    """q_prompt: bf16 CUDA tensor [P][layers][batch][heads][d]; trace_out: optional
+    int32 CUDA tensor [layers][batch][heads][min(fps_keep, P - recents)]."""
+    _check(_lib.bkv_prefill(_vp(h.ptr), _vp(q_prompt.data_ptr()), _i32(q_prompt.shape[0]),
+                            _i64(first_step), _vp(trace_out.data_ptr() if trace_out is not None else 0)),
+           "bkv_prefill")
 
 
 def bkv_coverage(h: Handle, q_future, out) -> None:

@@ -308,6 +308,40 @@ bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache
   return BKV_OK;
 }
 
+bkv_status bkv_prefill(bkv_handle h, const void* q_prompt, int32_t P, int64_t first_step,
+                       int32_t* trace_out) {
+  if (!h || !q_prompt || !aligned(q_prompt, 16) || (trace_out && !aligned(trace_out, 4)) || first_step < 0)
+    return BKV_ERR_INVALID_ARG;
+  const bkv_config& c = h->cfg;
+  if (P < 1 || P > c.max_cache) return BKV_ERR_INVALID_ARG;
+  if (h->last_step >= 0 || h->nb != 0 || h->nr != 0 || h->cache_len != 0) return BKV_ERR_STATE;
+  const int nr = P < h->n_rq ? P : h->n_rq;
+  const int N = P - nr;
+  const int m = N < c.fps_keep ? N : c.fps_keep;
+  if (bkv::prefill_smem_bytes(N > 0 ? N : 1) > kMaxSmem) return BKV_ERR_UNSUPPORTED;
+  bkv::PrefillParams p{};
+  p.q = static_cast<const uint4*>(q_prompt);
+  p.bq = h->bq();
+  p.rq = h->rq();
+  p.trace = trace_out;
+  p.status = h->status();
+  p.heads_total = h->heads_total;
+  p.first_step = first_step;
+  p.P = P;
+  p.N = N;
+  p.m = m;
+  p.nr = nr;
+  p.fps_cap = c.fps_cap;
+  p.n_rq = h->n_rq;
+  if (h->timed(BKV_K_PREFILL, [&] { return bkv::launch_prefill(p, h->stream); }) != cudaSuccess)
+    return BKV_ERR_CUDA;
+  h->nb = m;
+  h->nr = nr;
+  h->last_step = first_step + P - 1;
+  h->cache_len = P;
+  return BKV_OK;
+}
+
 bkv_status bkv_coverage(bkv_handle h, const void* q_future, int32_t n_future, double* out) {
   if (!h || !q_future || !out || n_future < 1 || !aligned(q_future, 16) || !aligned(out, 8))
     return BKV_ERR_INVALID_ARG;

@@ -73,6 +73,22 @@ struct CoverageParams {
 cudaError_t launch_coverage(const CoverageParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
+// prefill: initial beacons (FPS over the prompt's older queries) and recent ring
+struct PrefillParams {
+  const uint4* q;         // [P][heads_total][d] prompt queries, pre-RoPE
+  uint4* bq;              // [heads_total][fps_cap][d]
+  uint4* rq;              // [heads_total][n_rq][d]
+  int32_t* trace;         // optional [heads_total][m] picks in pick order
+  uint32_t* status;
+  int64_t heads_total;
+  int64_t first_step;     // position of prompt query 0
+  int P, N, m, nr;        // prompt length, FPS candidates, beacons kept, recents
+  int fps_cap, n_rq;
+};
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t s);
+size_t prefill_smem_bytes(int N);
+
+// ---------------------------------------------------------------------------
 // score + keep-set selection: persistent CTAs over the units
 struct ScoreParams {
   CUtensorMap kmap[kMaxLayers];  // per layer: K as 2-D [batch*kv_heads*max_cache][d] bf16

@@ -1,0 +1,380 @@
+// Prefill: each query head's initial observation state from the prompt
+// (BeaconKV reading notes §2.2: at prefill the first representatives are
+// sampled from the input queries). Of the P prompt queries, the last
+// nr = min(n_rq, P) go to the recent ring at their own positions and the
+// beacons are FPS (Algorithm 1) of the N = P - nr older ones, keeping
+// m = min(fps_keep, N). One CTA of 128 threads per head.
+//
+// FPS over N candidates (up to thousands) in O(N d m) instead of the O(N^2 d)
+// of a Gram matrix:
+//   * every candidate becomes a float32 unit vector u_j = (x_j 2^s_j) / ||.||
+//     (power-of-two scaling as in the FPS kernel, then rsqrtf); each warp
+//     takes one candidate at a time, lane l holding dimensions 4l..4l+3;
+//   * the mean cosine a_i = (1/N) sum_j cos(x_i, x_j) = u_i . mbar with
+//     mbar = (1/N) sum_j u_j, accumulated in float64 and rounded to float32;
+//   * every pick round refreshes S_j = max(S_j, u_j . u_r) in one pass.
+// Error bounds (relative to unit vectors, so absolute on cosines): u_j carries
+// <= 5.7e-7 per component (norm: 4 FMAs and a 5-level tree, gamma_9; rsqrtf
+// 2 ulp; one multiply), a float32 dot adds gamma_9; so |c32 - cos| <= 2e-6 and
+// |a32 - a64| <= 2e-6 plus the float64 reference's own summation error
+// (<= N 2^-53). The filters use kCosErr = 2e-5 and kMeanErr = 2.5e-5: a pick
+// is final when the float32 minimum beats every other candidate by twice the
+// bound; otherwise the exact float64 values of the close candidates (exact dot
+// products rounded once, IEEE division and square root, a_i summed left to
+// right) decide, ties to the lowest index.
+#include <climits>
+
+#include "bkv_internal.cuh"
+#include "exact_dot.cuh"
+
+namespace bkv {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
+constexpr float kCosErr = 2e-5f;
+constexpr float kMeanErr = 2.5e-5f;
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint32_t fkey(float v) {
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float unkey(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, off));
+  return v;
+}
+
+// Shared memory for N candidates.
+struct PfSmem {
+  float* inv;       // [N] 1 / ||x_j 2^s_j||
+  float* S;         // [N] mean cosine, then the running max cosine to the picks
+  uint8_t* E;       // [N] largest biased exponent of the row (sets s_j)
+  uint8_t* flag;    // [N] bit 0 picked, bit 1 close candidate
+  double* mpart;    // [kWarps][kD] per-warp sums of unit vectors
+  float* mvec;      // [kD] mean unit vector, float32
+  float* up;        // [kD] unit vector of the latest pick
+  double* xv;       // [kWarps][32] exact values, one chunk per warp
+  double* bestv;    // [kWarps]
+  int* besti;       // [kWarps]
+  uint32_t* red;    // [kWarps] reduction scratch
+  int* picks;       // [32]
+  int* ctl;         // [4] broadcast words
+};
+
+__host__ __device__ inline size_t pf_smem_bytes(int N) {
+  size_t b = (size_t)N * 10;
+  b = (b + 15) / 16 * 16;
+  return b + (size_t)kWarps * kD * 8 + kD * 4 * 2 + kWarps * 32 * 8 + kWarps * 8 + kWarps * 4 +
+         kWarps * 4 + 32 * 4 + 16 + 64;
+}
+
+__device__ inline PfSmem pf_carve(unsigned char* base, int N) {
+  PfSmem s;
+  size_t off = 0;
+  s.inv = reinterpret_cast<float*>(base + off);
+  off += (size_t)N * 4;
+  s.S = reinterpret_cast<float*>(base + off);
+  off += (size_t)N * 4;
+  s.E = base + off;
+  off += N;
+  s.flag = base + off;
+  off += N;
+  off = (off + 15) / 16 * 16;
+  s.mpart = reinterpret_cast<double*>(base + off);
+  off += (size_t)kWarps * kD * 8;
+  s.xv = reinterpret_cast<double*>(base + off);
+  off += (size_t)kWarps * 32 * 8;
+  s.bestv = reinterpret_cast<double*>(base + off);
+  off += kWarps * 8;
+  s.mvec = reinterpret_cast<float*>(base + off);
+  off += kD * 4;
+  s.up = reinterpret_cast<float*>(base + off);
+  off += kD * 4;
+  s.besti = reinterpret_cast<int*>(base + off);
+  off += kWarps * 4;
+  s.red = reinterpret_cast<uint32_t*>(base + off);
+  off += kWarps * 4;
+  s.picks = reinterpret_cast<int*>(base + off);
+  off += 32 * 4;
+  s.ctl = reinterpret_cast<int*>(base + off);
+  return s;
+}
+
+// exponent range and wideness of a bf16 row (for the exact dot products)
+__device__ void row_meta(const uint4* row, int& emin_out, bool& wide_out) {
+  int emin = INT_MAX, emax = INT_MIN;
+  for (int k = 0; k < kD; ++k) {
+    int sig, e, neg, nf;
+    decode_bf16(elem(row, k), sig, e, neg, nf);
+    if (sig != 0 && !nf) {
+      emin = min(emin, e);
+      emax = max(emax, e);
+    }
+  }
+  if (emin == INT_MAX) emin = emax = 0;
+  emin_out = emin;
+  wide_out = emax - emin > 20;
+}
+
+// the float64 cosine of the reference arithmetic; gii = exact G_ii
+__device__ double cos64_rows(const uint4* ri, int ei, bool wi, double gii, const uint4* rj) {
+  int ej;
+  bool wj;
+  row_meta(rj, ej, wj);
+  const double gjj = exact_dot(rj, rj, ej, ej, wj);
+  if (gii == 0.0 || gjj == 0.0) return 0.0;
+  const double g = exact_dot(ri, rj, ei, ej, wi || wj);
+  return __ddiv_rn(g, __dsqrt_rn(__dmul_rn(gii, gjj)));
+}
+
+__global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
+  extern __shared__ __align__(16) unsigned char pf_smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t head = blockIdx.x;
+  const int N = P.N, m = P.m;
+  PfSmem sm = pf_carve(pf_smem, N);
+  auto row = [&](int j) -> const uint4* { return P.q + ((int64_t)j * P.heads_total + head) * 16; };
+  uint4* bq = P.bq + head * P.fps_cap * 16;
+  uint4* rq = P.rq + head * P.n_rq * 16;
+
+  // ---- recent ring: prompt query P - nr + k at position first_step + P - nr + k
+  for (int idx = tid; idx < P.nr * 16; idx += kThreads) {
+    const int k = idx >> 4, part = idx & 15;
+    const int64_t tau = P.first_step + P.P - P.nr + k;
+    const int slot = (int)(((tau % P.n_rq) + P.n_rq) % P.n_rq);
+    rq[slot * 16 + part] = row(P.P - P.nr + k)[part];
+  }
+  if (N <= 0 || m <= 0) return;  // uniform: no beacons to sample
+  if (N <= m) {                   // every older query is kept in order
+    for (int idx = tid; idx < N * 16; idx += kThreads) bq[idx] = row(idx >> 4)[idx & 15];
+    if (P.trace)
+      for (int k = tid; k < m; k += kThreads) P.trace[head * m + k] = k < N ? k : -1;
+    return;
+  }
+
+  // lane's four components of candidate j as float32, scaled by 2^(127 - E_j)
+  auto load4 = [&](int j, float (&y)[4], uint32_t& emax) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(row(j)) + lane);
+    const uint32_t h[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
+    emax = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      emax = max(emax, (h[i] >> 7) & 0xFFu);
+      y[i] = __uint_as_float(h[i] << 16);
+    }
+  };
+  auto unit4 = [&](int j, float (&u)[4]) {
+    float y[4];
+    uint32_t e;
+    load4(j, y, e);
+    const float scale = __int_as_float(max(254 - (int)sm.E[j], 1) << 23);
+    const float iv = sm.inv[j];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[i] = __fmul_rn(__fmul_rn(y[i], scale), iv);
+  };
+
+  // ---- phase A: scaling, norms, flags, sum of unit vectors
+  double macc[4] = {0.0, 0.0, 0.0, 0.0};
+  bool bad = false;
+  for (int j = warp; j < N; j += kWarps) {
+    float y[4];
+    uint32_t e;
+    load4(j, y, e);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) e = max(e, __shfl_xor_sync(kFull, e, off));
+    bad |= e == 0xFFu;
+    const float scale = __int_as_float(max(254 - (int)e, 1) << 23);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[i] = __fmul_rn(y[i], scale);
+    float n2 = __fmul_rn(y[0], y[0]);
+    n2 = __fmaf_rn(y[1], y[1], n2);
+    n2 = __fmaf_rn(y[2], y[2], n2);
+    n2 = __fmaf_rn(y[3], y[3], n2);
+    n2 = warp_sum(n2);
+    const float iv = n2 > 0.f ? rsqrtf(n2) : 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) macc[i] = __dadd_rn(macc[i], (double)__fmul_rn(y[i], iv));
+    if (lane == 0) {
+      sm.inv[j] = iv;
+      sm.E[j] = (uint8_t)e;
+      sm.flag[j] = 0;
+    }
+  }
+  if (__syncthreads_or(bad) && tid == 0) latch(P.status, BKV_ERR_NONFINITE);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sm.mpart[warp * kD + 4 * lane + i] = macc[i];
+  __syncthreads();
+  {
+    double s = 0.0;
+    for (int w = 0; w < kWarps; ++w) s = __dadd_rn(s, sm.mpart[w * kD + tid]);
+    sm.mvec[tid] = __double2float_rn(__ddiv_rn(s, (double)N));
+  }
+  __syncthreads();
+
+  // ---- phase B: mean cosines a_j = u_j . mbar
+  for (int j = warp; j < N; j += kWarps) {
+    float u[4];
+    unit4(j, u);
+    float a = __fmul_rn(u[0], sm.mvec[4 * lane]);
+#pragma unroll
+    for (int i = 1; i < 4; ++i) a = __fmaf_rn(u[i], sm.mvec[4 * lane + i], a);
+    a = warp_sum(a);
+    if (lane == 0) sm.S[j] = a;
+  }
+  __syncthreads();
+
+  // ---- filtered argmin over the unpicked candidates; exact values decide close calls
+  // kind 0: mean cosine of candidate i; kind 1: running max cosine over picks[0, k)
+  auto choose = [&](float err, int kind, int k) -> int {
+    uint32_t key = 0xFFFFFFFFu;
+    for (int j = tid; j < N; j += kThreads)
+      if (!(sm.flag[j] & 1)) key = min(key, fkey(sm.S[j]));
+    key = __reduce_min_sync(kFull, key);
+    if (lane == 0) sm.red[warp] = key;
+    __syncthreads();
+    uint32_t all = sm.red[0];
+    for (int w = 1; w < kWarps; ++w) all = min(all, sm.red[w]);
+    const float lim = unkey(all) + 2.0f * err;
+    int cnt = 0, last = -1;
+    for (int j = tid; j < N; j += kThreads)
+      if (!(sm.flag[j] & 1) && sm.S[j] <= lim) {
+        ++cnt;
+        last = j;
+        sm.flag[j] |= 2;
+      }
+    const int holders = __syncthreads_count(cnt > 0);  // threads holding a close candidate
+    const int several = __syncthreads_count(cnt > 1);  // threads holding more than one
+    int pick;
+    if (holders == 1 && several == 0) {
+      if (cnt) sm.ctl[0] = last;
+      __syncthreads();
+      pick = sm.ctl[0];
+    } else {
+      // each warp evaluates the close candidates of its residue class exactly
+      double bv = 0.0;
+      int bi = -1;
+      for (int i = warp; i < N; i += kWarps) {
+        if (!(sm.flag[i] & 2)) continue;  // uniform across the warp
+        const uint4* ri = row(i);
+        int ei;
+        bool wi;
+        row_meta(ri, ei, wi);
+        const double gii = exact_dot(ri, ri, ei, ei, wi);
+        double v;
+        if (kind == 0) {
+          double acc = 0.0;  // sum_j cos64(i, j), left to right in j
+          for (int j0 = 0; j0 < N; j0 += 32) {
+            const int j = j0 + lane;
+            if (j < N) sm.xv[warp * 32 + lane] = cos64_rows(ri, ei, wi, gii, row(j));
+            __syncwarp();
+            if (lane == 0)
+              for (int q = 0; q < 32 && j0 + q < N; ++q) acc = __dadd_rn(acc, sm.xv[warp * 32 + q]);
+            __syncwarp();
+          }
+          v = __ddiv_rn(__shfl_sync(kFull, acc, 0), (double)N);
+        } else {
+          double mx = -__longlong_as_double(0x7ff0000000000000LL);
+          for (int q = lane; q < k; q += 32) {
+            const double c = cos64_rows(ri, ei, wi, gii, row(sm.picks[q]));
+            mx = c > mx ? c : mx;
+          }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            const double o = __shfl_xor_sync(kFull, mx, off);
+            mx = o > mx ? o : mx;
+          }
+          v = mx;
+        }
+        if (bi < 0 || v < bv) {  // i ascends within the warp: ties keep the lower index
+          bv = v;
+          bi = i;
+        }
+      }
+      if (lane == 0) {
+        sm.bestv[warp] = bv;
+        sm.besti[warp] = bi;
+      }
+      __syncthreads();
+      pick = -1;
+      double pv = 0.0;
+      for (int w = 0; w < kWarps; ++w) {
+        const int i = sm.besti[w];
+        if (i < 0) continue;
+        const double v = sm.bestv[w];
+        if (pick < 0 || v < pv || (v == pv && i < pick)) {
+          pick = i;
+          pv = v;
+        }
+      }
+      if (pick < 0) pick = 0;  // only with NaN inputs, which are latched
+    }
+    for (int j = tid; j < N; j += kThreads) sm.flag[j] &= 1;
+    __syncthreads();
+    return pick;
+  };
+
+  // ---- Algorithm 1
+  for (int k = 0; k < m; ++k) {
+    const int r = choose(k == 0 ? kMeanErr : kCosErr, k == 0 ? 0 : 1, k);
+    if (tid == 0) {
+      sm.picks[k] = r;
+      sm.flag[r] |= 1;
+    }
+    if (warp == 0) {
+      float u[4];
+      unit4(r, u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sm.up[4 * lane + i] = u[i];
+    }
+    __syncthreads();
+    if (k + 1 < m) {
+      for (int j = warp; j < N; j += kWarps) {
+        float u[4];
+        unit4(j, u);
+        float c = __fmul_rn(u[0], sm.up[4 * lane]);
+#pragma unroll
+        for (int i = 1; i < 4; ++i) c = __fmaf_rn(u[i], sm.up[4 * lane + i], c);
+        c = warp_sum(c);
+        if (lane == 0) sm.S[j] = k == 0 ? c : fmaxf(sm.S[j], c);
+      }
+      __syncthreads();
+    }
+  }
+
+  // ---- beacons: the picked rows in candidate order; the trace in pick order
+  if (P.trace)
+    for (int k = tid; k < m; k += kThreads) P.trace[head * m + k] = sm.picks[k];
+  for (int idx = tid; idx < m * 16; idx += kThreads) {
+    const int k = idx >> 4;
+    // the k-th smallest pick
+    int v = 0;
+    for (int q = 0; q < m; ++q) {
+      int rank = 0;
+      for (int q2 = 0; q2 < m; ++q2) rank += sm.picks[q2] < sm.picks[q];
+      if (rank == k) v = sm.picks[q];
+    }
+    bq[idx] = row(v)[idx & 15];
+  }
+}
+
+}  // namespace
+
+size_t prefill_smem_bytes(int N) { return pf_smem_bytes(N); }
+
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t s) {
+  if (p.heads_total <= 0) return cudaSuccess;
+  const size_t smem = pf_smem_bytes(p.N > 0 ? p.N : 1);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  prefill_kernel<<<(unsigned)p.heads_total, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace bkv

@@ -36,6 +36,7 @@ class Workload:
     global_noise: float = 0.1
     norm_sigma: float = 0.25
     aligned_keys: int = 64
+    cache_slots: int = 0  # cache capacity when a prompt may exceed budget + period (0: budget + period)
 
     @property
     def group(self) -> int:
@@ -43,7 +44,7 @@ class Workload:
 
     @property
     def max_cache(self) -> int:
-        return self.budget + self.period
+        return max(self.cache_slots, self.budget + self.period)
 
     @property
     def units(self) -> int:

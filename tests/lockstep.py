@@ -17,7 +17,10 @@ Agreement rules (per unit and eviction):
     oracle's order_free_layout of the returned set, and K/V follow it;
   * FPS traces after the eviction: identical pick order for every query head;
   * with coverage_n > 0, before each eviction: bkv_coverage over coverage_n
-    seeded future queries equals the oracle's coverage bit for bit (float64).
+    seeded future queries equals the oracle's coverage bit for bit (float64);
+  * with prefill = P > 0, the stream's first P steps arrive as one prompt
+    through bkv_prefill: its picks equal the oracle's prefill FPS trace, and
+    when P > budget the prompt is evicted at once (step P - 1, cache P).
 """
 
 from __future__ import annotations
@@ -70,7 +73,7 @@ def check_keep_set(gpu_kept, s_orc, orc_kept, L, prefix, recent, budget):
 def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "cpu",
                  steps: int | None = None, max_failures: int = 20,
                  query_hook=None, order_free: bool = False, pool: str = "max",
-                 coverage_n: int = 0) -> LockstepReport:
+                 coverage_n: int = 0, prefill: int = 0) -> LockstepReport:
     from kv_cache_eviction_head_gb300 import bkv
 
     dev = torch.device("cuda")
@@ -109,9 +112,135 @@ def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "c
         if len(rep.failures) < max_failures:
             rep.failures.append(msg)
 
+    def evict_and_check(t, cache_len):
+        # state before the eviction, byte for byte
+        nb_gpu = bkv.bkv_get_stats(h).beacons
+        for (l, b, kh) in sorted(live):
+            uo = oracles[(l, b, kh)]
+            for hg, st in enumerate(uo.heads):
+                gst = bkv.bkv_get_head_state(h, l, b, kh * G + hg)
+                ok = len(st.bq) == nb_gpu and all(
+                    np.array_equal(gst[i], r) for i, r in enumerate(st.bq))
+                ok = ok and all(np.array_equal(gst[w.fps_cap + tau % n_rq], r)
+                                for r, tau in st.rq)
+                if not ok:
+                    fail(f"t={t} unit {(l, b, kh)} head {hg}: beacon/recent state differs")
+                    live.discard((l, b, kh))
+                    break
+
+        if coverage_n > 0:
+            g = torch.Generator().manual_seed(seed * 7919 + t)
+            qf = (torch.randn(coverage_n, w.layers, w.batch, w.heads, d, generator=g)
+                  * torch.exp2(torch.randint(-3, 4, (coverage_n, 1, 1, w.heads, 1), generator=g).float())
+                  ).to(torch.bfloat16)
+            if query_hook is not None:
+                qf = torch.stack([query_hook(t + 1 + i, qf[i]) for i in range(coverage_n)])
+            cov = torch.empty(w.layers, w.batch, w.heads, coverage_n, dtype=torch.float64, device=dev)
+            bkv.bkv_coverage(h, qf.to(dev), cov)
+            cov_h = cov.cpu().numpy()
+            qf_bits = to_bits(qf)
+            for (l, b, kh) in sorted(live):
+                want = oracles[(l, b, kh)].coverage(
+                    [qf_bits[:, l, b, kh * G + hg] for hg in range(G)])
+                for hg in range(G):
+                    got = cov_h[l, b, kh * G + hg].tolist()
+                    rep.coverage_checked += coverage_n
+                    if got != want[hg]:
+                        i = next(i for i in range(coverage_n) if got[i] != want[hg][i])
+                        fail(f"t={t} unit {(l, b, kh)} head {hg}: coverage[{i}] "
+                             f"gpu {got[i]!r} orc {want[hg][i]!r}")
+                        live.discard((l, b, kh))
+                        break
+        bkv.bkv_evict(h, K, V, cache_len, t, kept)
+        bkv.bkv_sync(h)
+        rep.evictions += 1
+        scores = bkv.bkv_get_scores(h)
+        traces = bkv.bkv_get_fps_trace(h)
+        kept_h = kept.cpu().numpy()
+        L = cache_len
+        for (l, b, kh) in sorted(live):
+            uo = oracles[(l, b, kh)]
+            s_orc, _ = uo.scores(t)
+            s_gpu = scores[l, b, kh, :L].astype(np.float64)
+            err = np.abs(s_gpu - s_orc)
+            tol = SCORE_ATOL + SCORE_RTOL * np.abs(s_orc)
+            rel = float(np.max(err / np.maximum(np.abs(s_orc), 1e-30)))
+            rep.max_score_rel = max(rep.max_score_rel, rel)
+            if np.any(err > tol):
+                j = int(np.argmax(err - tol))
+                fail(f"t={t} unit {(l, b, kh)}: score[{j}] gpu {s_gpu[j]:.9g} orc {s_orc[j]:.9g}")
+                live.discard((l, b, kh))
+                continue
+            orc_kept = select_keep(s_orc, L, w.prefix, w.recent, w.budget)
+            g_layout = kept_h[l, b, kh].tolist()
+            g_kept = sorted(g_layout) if order_free else g_layout
+            why = check_keep_set(g_kept, s_orc, orc_kept, L, w.prefix, w.recent, w.budget)
+            if not why and order_free and g_layout != order_free_layout(g_kept, w.budget):
+                why = "order-free layout differs from the holes-from-the-tail rule"
+            if why:
+                fail(f"t={t} unit {(l, b, kh)}: {why}")
+                live.discard((l, b, kh))
+                continue
+            if g_kept != orc_kept:
+                rep.kept_adopted += 1
+            res = uo.evict(t, kept_override=g_kept, score=s_orc)
+            kg = to_bits(K[l][b, kh, :w.budget])
+            vg = to_bits(V[l][b, kh, :w.budget])
+            if not (np.array_equal(kg, np.stack(uo.K)) and np.array_equal(vg, np.stack(uo.V))):
+                fail(f"t={t} unit {(l, b, kh)}: compacted K/V differ")
+                live.discard((l, b, kh))
+                continue
+            for hg, tr in enumerate(res.traces):
+                want = list(tr) + [-1] * (w.fps_keep - len(tr))
+                got = traces[l, b, kh * G + hg].tolist()
+                rep.fps_heads_checked += 1
+                if got != want:
+                    fail(f"t={t} unit {(l, b, kh)} head {hg}: FPS trace {got} != {want}")
+                    live.discard((l, b, kh))
+                    break
+            rep.units_checked += 1
+
     cache_len = 0
+    start = 0
     try:
-        for t in range(steps):
+        if prefill > 0:
+            # the stream's first `prefill` steps arrive as one prompt
+            qs_l = []
+            for t in range(prefill):
+                q = stream.queries()
+                if query_hook is not None:
+                    q = query_hook(t, q)
+                k, v = stream.keys_values(t)
+                kd, vd = k.to(dev), v.to(dev)
+                for l in range(w.layers):
+                    K[l][:, :, t] = kd[l]
+                    V[l][:, :, t] = vd[l]
+                qs_l.append(q)
+                ks, vs = to_bits(k[l_idx, b_idx, kh_idx]), to_bits(v[l_idx, b_idx, kh_idx])
+                for i, u in enumerate(sample_units):
+                    oracles[u].append_kv(ks[i], vs[i], t)
+            qp = torch.stack(qs_l)                                  # [P][layers][batch][heads][d]
+            nr0 = min(n_rq, prefill)
+            m0 = min(w.fps_keep, prefill - nr0)
+            tr = torch.full((w.layers, w.batch, w.heads, max(m0, 1)), -7, dtype=torch.int32, device=dev)
+            bkv.bkv_prefill(h, qp.to(dev), 0, tr if m0 > 0 else None)
+            qp_bits = to_bits(qp[:, l_idx, b_idx])                 # [P][units][heads][d]
+            tr_h = tr.cpu().numpy()
+            for i, (l, b, kh) in enumerate(sample_units):
+                uo = oracles[(l, b, kh)]
+                uo.prefill([qp_bits[:, i, kh * G + hg] for hg in range(G)], 0)
+                for hg, st in enumerate(uo.heads):
+                    got = tr_h[l, b, kh * G + hg, :m0].tolist() if m0 > 0 else []
+                    rep.fps_heads_checked += 1
+                    if got != list(st.trace):
+                        fail(f"prefill unit {(l, b, kh)} head {hg}: picks {got} != {list(st.trace)}")
+                        live.discard((l, b, kh))
+            cache_len = prefill
+            start = prefill
+            if prefill > w.budget:                                  # evict the prompt down to the budget
+                evict_and_check(prefill - 1, cache_len)
+                cache_len = w.budget
+        for t in range(start, steps):
             q = stream.queries()
             if query_hook is not None:
                 q = query_hook(t, q)
@@ -133,92 +262,7 @@ def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "c
             if cache_len < w.budget + w.period:
                 continue
 
-            # state before the eviction, byte for byte
-            nb_gpu = bkv.bkv_get_stats(h).beacons
-            for (l, b, kh) in sorted(live):
-                uo = oracles[(l, b, kh)]
-                for hg, st in enumerate(uo.heads):
-                    gst = bkv.bkv_get_head_state(h, l, b, kh * G + hg)
-                    ok = len(st.bq) == nb_gpu and all(
-                        np.array_equal(gst[i], r) for i, r in enumerate(st.bq))
-                    ok = ok and all(np.array_equal(gst[w.fps_cap + tau % n_rq], r)
-                                    for r, tau in st.rq)
-                    if not ok:
-                        fail(f"t={t} unit {(l, b, kh)} head {hg}: beacon/recent state differs")
-                        live.discard((l, b, kh))
-                        break
-
-            if coverage_n > 0:
-                g = torch.Generator().manual_seed(seed * 7919 + t)
-                qf = (torch.randn(coverage_n, w.layers, w.batch, w.heads, d, generator=g)
-                      * torch.exp2(torch.randint(-3, 4, (coverage_n, 1, 1, w.heads, 1), generator=g).float())
-                      ).to(torch.bfloat16)
-                if query_hook is not None:
-                    qf = torch.stack([query_hook(t + 1 + i, qf[i]) for i in range(coverage_n)])
-                cov = torch.empty(w.layers, w.batch, w.heads, coverage_n, dtype=torch.float64, device=dev)
-                bkv.bkv_coverage(h, qf.to(dev), cov)
-                cov_h = cov.cpu().numpy()
-                qf_bits = to_bits(qf)
-                for (l, b, kh) in sorted(live):
-                    want = oracles[(l, b, kh)].coverage(
-                        [qf_bits[:, l, b, kh * G + hg] for hg in range(G)])
-                    for hg in range(G):
-                        got = cov_h[l, b, kh * G + hg].tolist()
-                        rep.coverage_checked += coverage_n
-                        if got != want[hg]:
-                            i = next(i for i in range(coverage_n) if got[i] != want[hg][i])
-                            fail(f"t={t} unit {(l, b, kh)} head {hg}: coverage[{i}] "
-                                 f"gpu {got[i]!r} orc {want[hg][i]!r}")
-                            live.discard((l, b, kh))
-                            break
-            bkv.bkv_evict(h, K, V, cache_len, t, kept)
-            bkv.bkv_sync(h)
-            rep.evictions += 1
-            scores = bkv.bkv_get_scores(h)
-            traces = bkv.bkv_get_fps_trace(h)
-            kept_h = kept.cpu().numpy()
-            L = cache_len
-            for (l, b, kh) in sorted(live):
-                uo = oracles[(l, b, kh)]
-                s_orc, _ = uo.scores(t)
-                s_gpu = scores[l, b, kh, :L].astype(np.float64)
-                err = np.abs(s_gpu - s_orc)
-                tol = SCORE_ATOL + SCORE_RTOL * np.abs(s_orc)
-                rel = float(np.max(err / np.maximum(np.abs(s_orc), 1e-30)))
-                rep.max_score_rel = max(rep.max_score_rel, rel)
-                if np.any(err > tol):
-                    j = int(np.argmax(err - tol))
-                    fail(f"t={t} unit {(l, b, kh)}: score[{j}] gpu {s_gpu[j]:.9g} orc {s_orc[j]:.9g}")
-                    live.discard((l, b, kh))
-                    continue
-                orc_kept = select_keep(s_orc, L, w.prefix, w.recent, w.budget)
-                g_layout = kept_h[l, b, kh].tolist()
-                g_kept = sorted(g_layout) if order_free else g_layout
-                why = check_keep_set(g_kept, s_orc, orc_kept, L, w.prefix, w.recent, w.budget)
-                if not why and order_free and g_layout != order_free_layout(g_kept, w.budget):
-                    why = "order-free layout differs from the holes-from-the-tail rule"
-                if why:
-                    fail(f"t={t} unit {(l, b, kh)}: {why}")
-                    live.discard((l, b, kh))
-                    continue
-                if g_kept != orc_kept:
-                    rep.kept_adopted += 1
-                res = uo.evict(t, kept_override=g_kept, score=s_orc)
-                kg = to_bits(K[l][b, kh, :w.budget])
-                vg = to_bits(V[l][b, kh, :w.budget])
-                if not (np.array_equal(kg, np.stack(uo.K)) and np.array_equal(vg, np.stack(uo.V))):
-                    fail(f"t={t} unit {(l, b, kh)}: compacted K/V differ")
-                    live.discard((l, b, kh))
-                    continue
-                for hg, tr in enumerate(res.traces):
-                    want = list(tr) + [-1] * (w.fps_keep - len(tr))
-                    got = traces[l, b, kh * G + hg].tolist()
-                    rep.fps_heads_checked += 1
-                    if got != want:
-                        fail(f"t={t} unit {(l, b, kh)} head {hg}: FPS trace {got} != {want}")
-                        live.discard((l, b, kh))
-                        break
-                rep.units_checked += 1
+            evict_and_check(t, cache_len)
             cache_len = w.budget
         rep.rows_moved = int(bkv.bkv_get_stats(h).rows_moved)
     finally:

@@ -270,6 +270,44 @@ def test_coverage_qwen3_4b_b192_full_size_sampled_units():
     assert rep.coverage_checked == len(units) * w.group * 8 * rep.evictions
 
 
+# ---------------------------------------------------------------------------- prefill
+
+@pytest.mark.parametrize("P", [10, 20, 100, 144])
+def test_prefill_tiny(P):
+    """Prefill over the stream's first P steps: all recent (P <= n_rq), every
+    older query kept (N <= fps_keep), FPS over 84 older queries, and a prompt
+    of budget + period evicted at once; the stream then continues in lockstep."""
+    w = TINY.with_(steps=320)
+    rep = run_lockstep(w, seed=0xBEAD2 + P, prefill=P)
+    assert_clean(rep, min_evictions=4)
+
+
+def test_prefill_long_prompt_then_large_eviction():
+    """A 700-step prompt: FPS over 684 older queries per head, then one
+    eviction from 700 slots to 128 (572 drops: the radix select) and decoding."""
+    w = TINY.with_(cache_slots=700, steps=800)
+    rep = run_lockstep(w, seed=0xBEAD3, prefill=700)
+    assert_clean(rep, min_evictions=4)
+
+
+def test_prefill_gqa7_wide_exponents():
+    # 96 prompt steps keep the FPS phase of a plain stream: at each eviction a
+    # head holds 16 beacons + 16 recents, so 7 heads make 224 observation rows
+    # (a prompt of 90 would leave 22 + 16 per head, 266 rows: beyond the 256
+    # the score kernel takes)
+    w = TINY.with_(heads=7, kv_heads=1, steps=260)
+    rep = run_lockstep(w, seed=0xBEAD4, prefill=96, query_hook=wide_queries)
+    assert_clean(rep, min_evictions=3)
+
+
+def test_prefill_qwen3_4b_b192_full_size_sampled_units():
+    w = WORKLOADS["qwen3_4b_b192"]
+    units = [(0, 0, 0), (35, 191, 7)]
+    rep = run_lockstep(w, seed=0xBEAD5, sample_units=units, gen_device="cuda",
+                       steps=w.max_cache + w.period, prefill=200)
+    assert_clean(rep, min_evictions=2)
+
+
 def wide_queries(t, q):
     """Replaces some queries by vectors whose exponents span far more than 20
     binades (FPS's wide exact-sum path), by zero rows and by exact duplicates."""
