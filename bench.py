@@ -400,6 +400,30 @@ def run_ours(args, w):
                "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"]}
 
     bkv.bkv_destroy(h)
+
+    # ---- prefill: initial beacons from a prompt of args.prefill queries (timed alone)
+    prefill = None
+    if args.prefill > 0:
+        P = min(args.prefill, w.max_cache)
+        gq = torch.Generator(device=dev).manual_seed(7)
+        qp = torch.randn(P, w.layers, w.batch, w.heads, w.d, generator=gq, device=dev).to(torch.bfloat16)
+        ms = []
+        for rep in range(4):
+            ws2 = torch.empty(bkv.bkv_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+            h2 = bkv.bkv_create(cfg, ws2, cs)
+            pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            pa.record(cs)
+            bkv.bkv_prefill(h2, qp, 0)
+            pb.record(cs)
+            torch.cuda.synchronize(dev)
+            bkv.bkv_sync(h2)
+            bkv.bkv_destroy(h2)
+            if rep > 0:
+                ms.append(pa.elapsed_time(pb))
+        N = P - min(w.fps_cap - w.fps_keep, P)
+        prefill = {"prompt": P, "older_queries_per_head": N, "ms": statistics.median(ms),
+                   "heads": heads_total, "candidates_per_s": heads_total * N / (statistics.median(ms) / 1e3)}
+        del qp
     del K, V
     torch.cuda.empty_cache()
 
@@ -445,6 +469,7 @@ def run_ours(args, w):
             "kernels": kernels,
             "clocks": clocks,
             "coverage": coverage,
+            "prefill": prefill,
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
@@ -537,6 +562,8 @@ def main():
                     help="aggregation of the attention weights over observation rows")
     ap.add_argument("--fps-keep", type=int, default=None,
                     help="beacons kept per head (recent queries = 32 - this), Table 1's splits")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="also time bkv_prefill over a prompt of this many steps (fresh state)")
     ap.add_argument("--coverage", type=int, default=0,
                     help="also time bkv_coverage over this many future queries (diagnostic)")
     ap.add_argument("--no-e2e", action="store_true")
