@@ -558,6 +558,7 @@ def main():
     ap.add_argument("--ref-units-per-step", type=int, default=32)
     ap.add_argument("--order-free", action="store_true",
                     help="order-free compaction (BKV_FLAG_ORDER_FREE) instead of slot order")
+    ap.add_argument("--budget", type=int, default=None, help="override the workload's budget")
     ap.add_argument("--pool", choices=["max", "mean"], default="max",
                     help="aggregation of the attention weights over observation rows")
     ap.add_argument("--fps-keep", type=int, default=None,
@@ -577,6 +578,8 @@ def main():
         w = w.with_(batch=args.batch, name=f"{w.name}_batch{args.batch}")
     if args.fps_keep is not None:
         w = w.with_(fps_keep=args.fps_keep, name=f"{w.name}_keep{args.fps_keep}")
+    if args.budget is not None:
+        w = w.with_(budget=args.budget, name=f"{w.name}_budget{args.budget}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
