@@ -152,7 +152,9 @@ bkv_status bkv_append_queries(bkv_handle h, const void* q_pre, int64_t step);
  * On completion slots [0, budget) of every unit hold K[kept] / V[kept];
  * slots [budget, cache_len) are left with unspecified contents. Then every
  * query head's beacons become FPS(beacons + recents, fps_keep) and its recent
- * ring is emptied. BKV_ERR_UNSUPPORTED if G * (beacons + recents) > 256;
+ * ring is emptied. Units with more than 256 observation rows are scored in
+ * row chunks of at most 256 (same result); BKV_ERR_UNSUPPORTED if
+ * G * (beacons + recents) > 2048;
  * BKV_ERR_INVALID_ARG with BKV_FLAG_ORDER_FREE if recent > cache_len - budget. */
 bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache_len,
                      int64_t step, int32_t* kept);

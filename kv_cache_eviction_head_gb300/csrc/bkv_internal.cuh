@@ -13,7 +13,7 @@ namespace bkv {
 
 constexpr int kD = 128;             // head dimension the kernels implement
 constexpr int kMaxLayers = 128;     // per-layer K/V pointers travel in the launch parameters
-constexpr int kMaxObsRows = 256;    // observation rows per unit (G * (beacons + recents))
+constexpr int kMaxObsRows = 2048;   // observation rows per unit (G * (beacons + recents)), in chunks of <= 256
 constexpr int kMaxFpsCap = 32;      // one warp lane per FPS candidate
 constexpr int kRopePairs = kD / 2;
 

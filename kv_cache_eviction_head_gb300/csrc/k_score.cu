@@ -464,7 +464,8 @@ constexpr int kPfRows = 512;                      // L2 prefetch lead of the cop
 constexpr int kPfPieceRows = 64;                  // rows per L2 prefetch
 
 struct Layout {
-  int R, Rp16, mtiles, qrows, rows64;  // rows, rows to 16, M tiles, rows allocated, rows to 64
+  int Rtot, chunks;                    // observation rows of a unit, row chunks of <= 256
+  int R, Rp16, mtiles, qrows, rows64;  // rows per chunk, to 16, M tiles, rows allocated, rows to 64
   int ntiles, Lp, stages, bufcols, cbufs, scbufs, D;
   size_t q_hi, q_lo, kst, cst, sc, lse, lim, part, rowinfo, drops, bars, misc, total;
 };
@@ -476,8 +477,13 @@ struct Layout {
 // compacting in slot order, two chunks (and more K stages) for the order-free
 // compaction, which moves at most L - budget rows; two score buffers (one
 // when nothing else fits).
-__host__ __device__ inline Layout make_layout(int R, int L, int nr, int budget, int compact) {
+__host__ __device__ inline Layout make_layout(int Rtot, int L, int nr, int budget, int compact) {
   Layout s;
+  // more than 256 rows run as equal chunks (the last one padded with masked
+  // zero rows): two TMEM buffers of two M tiles hold 256 rows
+  s.Rtot = Rtot;
+  s.chunks = (Rtot + 255) / 256 > 0 ? (Rtot + 255) / 256 : 1;
+  const int R = (Rtot + s.chunks - 1) / s.chunks;
   s.R = R;
   s.Rp16 = (R + 15) & ~15;
   s.mtiles = R > 128 ? 2 : 1;
@@ -488,8 +494,8 @@ __host__ __device__ inline Layout make_layout(int R, int L, int nr, int budget, 
   s.bufcols = (s.mtiles > 1 || s.Rp16 > 128) ? 256 : 128;
   s.D = L - budget;
   const size_t qbytes = ((size_t)s.qrows * 256 + 1023) / 1024 * 1024;  // two 128-byte slabs per row
-  const size_t small = (size_t)s.rows64 * 8 + (size_t)s.qrows * 16 + (size_t)s.qrows * 8 +
-                       2 * (size_t)s.D * 4 + 16 + 64 * 8 + kMiscBytes + 64;
+  const size_t small = (size_t)s.rows64 * 4 * (1 + s.chunks) + (size_t)s.qrows * 16 +
+                       (size_t)s.chunks * s.qrows * 8 + 2 * (size_t)s.D * 4 + 16 + 64 * 8 + kMiscBytes + 64;
   const size_t cap = 227 * 1024 - 1024;  // 1 KB kept for aligning the dynamic base
   const size_t scb = (size_t)s.Lp * 4;
   static const int plans[][3] = {{4, 0, 2}, {3, 0, 2}, {2, 0, 2}, {2, 0, 1}};          // no compaction
@@ -521,12 +527,12 @@ __host__ __device__ inline Layout make_layout(int R, int L, int nr, int budget, 
   off += (size_t)s.scbufs * scb;
   s.lse = off;
   off += (size_t)s.rows64 * 4;
-  s.lim = off;
-  off += (size_t)s.rows64 * 4;
+  s.lim = off;  // [chunks][rows64]
+  off += (size_t)s.chunks * s.rows64 * 4;
   s.part = off;
   off += (size_t)s.qrows * 16;
-  s.rowinfo = off;
-  off += (size_t)s.qrows * 8;
+  s.rowinfo = off;  // [chunks][qrows]
+  off += (size_t)s.chunks * s.qrows * 8;
   s.drops = off;
   off += 2 * (size_t)s.D * 4 + 16;
   s.bars = (off + 7) & ~(size_t)7;
@@ -609,22 +615,29 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   // zero both row buffers once: padding rows stay zero for the whole launch
   for (int i = tid; i < (int)(2 * (lay.q_lo - lay.q_hi) / 16); i += kThreads)
     reinterpret_cast<uint4*>(q_hi)[i] = make_uint4(0, 0, 0, 0);
-  for (int r = tid; r < lay.rows64; r += kThreads) {
+  // per-launch tables, chunk by chunk: the key bound of each row (0 masks
+  // padding rows) and each row's source (x = -1: a zero padding row)
+  for (int i = tid; i < lay.chunks * lay.rows64; i += kThreads) {
+    const int rl = i % lay.rows64, r = (i / lay.rows64) * R + rl;
     int bound = 0;
-    if (r < R) {
+    if (rl < R && r < lay.Rtot) {
       const int w = r % per_head;
       bound = w < P.nb ? L : L - P.nr + (w - P.nb) + 1;
     }
-    lim[r] = bound;
+    lim[i] = bound;
   }
-  // per-launch table: each observation row's source
-  for (int r = tid; r < R; r += kThreads) {
+  for (int i = tid; i < lay.chunks * lay.qrows; i += kThreads) {
+    const int rl = i % lay.qrows, r = (i / lay.qrows) * R + rl;
+    if (rl >= R || r >= lay.Rtot) {
+      rowinfo[i] = make_int2(-1, 0);
+      continue;
+    }
     const int gi = r / per_head, w = r % per_head;
     if (w < P.nb) {
-      rowinfo[r] = make_int2((gi * P.fps_cap + w) * 16, 0);
+      rowinfo[i] = make_int2((gi * P.fps_cap + w) * 16, 0);
     } else {
       const int kq = w - P.nb;
-      rowinfo[r] = make_int2(((gi * P.n_rq + (P.ring_first + kq) % P.n_rq) * 16) | (1 << 30), 1 + kq);
+      rowinfo[i] = make_int2(((gi * P.n_rq + (P.ring_first + kq) % P.n_rq) * 16) | (1 << 30), 1 + kq);
     }
   }
   const uint32_t ncols = 2 * (uint32_t)lay.bufcols;
@@ -643,16 +656,18 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
     unit_geom(blockIdx.x + it * gridDim.x, P.batch, P.kv_heads, layer, seq, kvh);
     return ((int64_t)layer * P.batch + seq) * (P.kv_heads * P.group) + (int64_t)kvh * P.group;
   };
-  // source row of observation row r and its RoPE table row
-  auto row_src = [&](int64_t head0, int r, int& prow) -> const uint4* {
-    const int2 info = rowinfo[r];
+  // source of row r of chunk c (nullptr: zero padding) and its RoPE table row
+  auto row_src = [&](int64_t head0, int c, int r, int& prow) -> const uint4* {
+    const int2 info = rowinfo[c * lay.qrows + r];
     prow = info.y;
+    if (info.x < 0) return nullptr;
     const uint4* base = (info.x & (1 << 30)) ? P.rq + head0 * P.n_rq * 16 : P.bq + head0 * P.fps_cap * 16;
     return base + (info.x & ~(1 << 30));
   };
-  // Rotated observation rows of unit `it`, split into bf16 hi + lo, written in
-  // the SWIZZLE_128B K-major layout; thread t of n builds items t, t + n, ...
-  auto build_rows = [&](int it, int t, int n) {
+  // Rotated observation rows of chunk c of unit `it`, split into bf16 hi + lo,
+  // written in the SWIZZLE_128B K-major layout; thread t of n builds items
+  // t, t + n, ...
+  auto build_rows = [&](int it, int c, int t, int n) {
     constexpr int kBatch = 4;  // items per thread with loads in flight together
     const int64_t head0 = head_base(it);
     for (int base = 0; base < R * 8; base += n * kBatch) {
@@ -661,10 +676,14 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
 #pragma unroll
       for (int bi = 0; bi < kBatch; ++bi) {
         const int idx = base + t + n * bi;
+        xl[bi] = xh[bi] = make_uint4(0, 0, 0, 0);
+        prow[bi] = 0;
         if (idx < R * 8) {
-          const uint4* src = row_src(head0, idx >> 3, prow[bi]);
-          xl[bi] = src[idx & 7];
-          xh[bi] = src[(idx & 7) + 8];
+          const uint4* src = row_src(head0, c, idx >> 3, prow[bi]);
+          if (src) {
+            xl[bi] = src[idx & 7];
+            xh[bi] = src[(idx & 7) + 8];
+          }
         }
       }
 #pragma unroll
@@ -717,7 +736,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
         int layer, seq, kvh;
         unit_geom(blockIdx.x + it * gridDim.x, P.batch, P.kv_heads, layer, seq, kvh);
         const int row0 = (seq * P.kv_heads + kvh) * P.max_cache;
-        for (int s = 0; s < 2 * T; ++s) {
+        for (int s2 = 0; s2 < 2 * T * lay.chunks; ++s2) {
+          const int s = s2 % (2 * T);  // each row chunk runs both passes
           if (g >= S && !mbar_wait(&kempty[st], kph ^ 1u, ctl, P.status)) {
             ok = false;
             break;
@@ -753,51 +773,54 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       const uint32_t qh = smem_u32(q_hi), ql = smem_u32(q_lo);
       const uint32_t slab_q = (uint32_t)lay.qrows * 128;  // bytes of one 64-column slab of the rows
       const uint32_t id1 = idesc_bf16(128, 128), id2 = idesc_bf16(128, lay.Rp16);
+      int ci = 0;  // row chunks started
       for (int it = 0; it < mine && ok; ++it) {
-        ok = mbar_wait(qready, (uint32_t)(it & 1), ctl, P.status);
-        for (int s = 0; s < 2 * T && ok; ++s, ++g) {
-          const int b = (int)(g & 1);
-          ok = mbar_wait(&kfull[st], kph, ctl, P.status);
-          if (ok && g >= 2) ok = mbar_wait(&tempty[b], (uint32_t)(((g >> 1) + 1) & 1), ctl, P.status);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t kb = smem_u32(kst + (size_t)st * kTileBytes);
-          const uint32_t d = tmem + (uint32_t)(b * lay.bufcols);
-          if (s < T) {
-            for (int mt = 0; mt < lay.mtiles; ++mt) {
-#pragma unroll
+        for (int c = 0; c < lay.chunks && ok; ++c, ++ci) {
+          ok = mbar_wait(qready, (uint32_t)(ci & 1), ctl, P.status);
+          for (int s = 0; s < 2 * T && ok; ++s, ++g) {
+            const int b = (int)(g & 1);
+            ok = mbar_wait(&kfull[st], kph, ctl, P.status);
+            if (ok && g >= 2) ok = mbar_wait(&tempty[b], (uint32_t)(((g >> 1) + 1) & 1), ctl, P.status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t kb = smem_u32(kst + (size_t)st * kTileBytes);
+            const uint32_t d = tmem + (uint32_t)(b * lay.bufcols);
+            if (s < T) {
+              for (int mt = 0; mt < lay.mtiles; ++mt) {
+  #pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                  const uint32_t qbase = (part ? ql : qh) + (uint32_t)(mt ? lay.Rp16 - 128 : 0) * 128;
+  #pragma unroll
+                  for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (uint32_t)(kk & 3) * 32;
+                    const uint64_t a = sw128_desc(qbase + (uint32_t)(kk >> 2) * slab_q + off);
+                    const uint64_t bd = sw128_desc(kb + (uint32_t)(kk >> 2) * kSlabBytes + off);
+                    umma_bf16(d + (uint32_t)mt * 128, a, bd, id1, (part | kk) ? 1u : 0u);
+                  }
+                }
+              }
+            } else {
+  #pragma unroll
               for (int part = 0; part < 2; ++part) {
-                const uint32_t qbase = (part ? ql : qh) + (uint32_t)(mt ? lay.Rp16 - 128 : 0) * 128;
-#pragma unroll
+                const uint32_t qbase = part ? ql : qh;
+  #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                   const uint32_t off = (uint32_t)(kk & 3) * 32;
-                  const uint64_t a = sw128_desc(qbase + (uint32_t)(kk >> 2) * slab_q + off);
-                  const uint64_t bd = sw128_desc(kb + (uint32_t)(kk >> 2) * kSlabBytes + off);
-                  umma_bf16(d + (uint32_t)mt * 128, a, bd, id1, (part | kk) ? 1u : 0u);
+                  const uint64_t a = sw128_desc(kb + (uint32_t)(kk >> 2) * kSlabBytes + off);
+                  const uint64_t bd = sw128_desc(qbase + (uint32_t)(kk >> 2) * slab_q + off);
+                  umma_bf16(d, a, bd, id2, (part | kk) ? 1u : 0u);
                 }
               }
             }
-          } else {
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-              const uint32_t qbase = part ? ql : qh;
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (uint32_t)(kk & 3) * 32;
-                const uint64_t a = sw128_desc(kb + (uint32_t)(kk >> 2) * kSlabBytes + off);
-                const uint64_t bd = sw128_desc(qbase + (uint32_t)(kk >> 2) * slab_q + off);
-                umma_bf16(d, a, bd, id2, (part | kk) ? 1u : 0u);
-              }
+            umma_commit(&kempty[st]);
+            umma_commit(&tfull[b]);
+            if (++st == S) {
+              st = 0;
+              kph ^= 1u;
             }
           }
-          umma_commit(&kempty[st]);
-          umma_commit(&tfull[b]);
-          if (++st == S) {
-            st = 0;
-            kph ^= 1u;
-          }
+          if (ok) umma_commit(qfree);  // arrives when every MMA that read this chunk's rows is done
         }
-        if (ok) umma_commit(qfree);  // arrives when every MMA that read this unit's rows is done
       }
       // after an abort, let the MMAs already issued finish before the TMEM is freed
       if (!ok && g > 0) {
@@ -979,15 +1002,17 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       }
     } else {
       // ---------------------------------------------------------- L2 warmer
-      // Pulls the next unit's source rows into L2 while the current unit is
-      // scored, so the row build at the unit boundary reads from L2.
-      for (int it = 0; it + 1 < mine; ++it) {
-        const bool ok = __all_sync(kFull, mbar_wait(qready, (uint32_t)(it & 1), ctl, P.status));
+      // Pulls the next row chunk's source rows into L2 while the current one
+      // is scored, so the row build at the chunk boundary reads from L2.
+      const int nchunks = mine * lay.chunks;
+      for (int ci = 0; ci + 1 < nchunks; ++ci) {
+        const bool ok = __all_sync(kFull, mbar_wait(qready, (uint32_t)(ci & 1), ctl, P.status));
         if (!ok) break;
-        const int64_t h1 = head_base(it + 1);
+        const int64_t h1 = head_base((ci + 1) / lay.chunks);
         for (int r = lane; r < R; r += 32) {
           int pr;
-          const char* src = reinterpret_cast<const char*>(row_src(h1, r, pr));
+          const char* src = reinterpret_cast<const char*>(row_src(h1, (ci + 1) % lay.chunks, r, pr));
+          if (!src) continue;
           asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
           asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128));
         }
@@ -1025,182 +1050,199 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
     const int et = tid - 128 - grp * kEpiThreads, q = warp & 3;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const float neg_inf = __int_as_float(0xff800000u);
-    const float inv_rows = 1.0f / (float)R;  // mean pooling
+    const float inv_rows = 1.0f / (float)lay.Rtot;  // mean pooling
+    const int C = lay.chunks;
     long long g = 0;
     bool ok = true;
+    int ci = 0;                // row chunks done
     const int bt = tid - 128;  // 0..255 over both groups, for the row build
-    if (mine > 0) build_rows(0, bt, 2 * kEpiThreads);
+    if (mine > 0) build_rows(0, 0, bt, 2 * kEpiThreads);
     for (int it = 0; it < mine && ok; ++it) {
       const int b_sc = it % NSC;
       float* s_u = sc + (size_t)b_sc * lay.Lp;
-      float run_m[2] = {neg_inf, neg_inf}, run_z[2] = {0.f, 0.f};
-      for (int s = 0; s < 2 * T && ok; ++s, ++g) {
-        const int b = (int)(g & 1);
-        if (b == grp) {
-          ok = __all_sync(kFull, mbar_wait(&tfull[b], (uint32_t)((g >> 1) & 1), ctl, P.status));
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t col0 = tmem + lane_base + (uint32_t)(b * lay.bufcols);
-          const int kt = s < T ? s : 2 * T - 1 - s;
-          if (s < T) {
-            // pass 1: this thread owns observation row et (and a row of the second M tile)
-            for (int mt = 0; mt < lay.mtiles; ++mt) {
-              const int row = mt ? lay.Rp16 - 128 + et : et;
-              // The second M tile overlaps the first on rows below 128. tcgen05.ld
-              // is warp-collective (.sync.aligned), so only whole warps may skip
-              // it; lanes holding a duplicate row load and discard (bound 0
-              // masks every key, which leaves their running max and sum as is).
-              const bool dup = mt && row < 128;
-              if (__all_sync(kFull, dup)) continue;
-              const int bound = dup ? 0 : lim[row] - kt * kTileKeys;  // keys [0, bound) are visible
-#pragma unroll
-              for (int h = 0; h < 4; h += 2) {
-                float v[64];
-                tmem_ld32(col0 + (uint32_t)(mt * 128 + h * 32), *reinterpret_cast<float(*)[32]>(&v[0]));
-                tmem_ld32(col0 + (uint32_t)(mt * 128 + h * 32 + 32), *reinterpret_cast<float(*)[32]>(&v[32]));
-                tmem_wait_ld();
-                if (bound < (h + 2) * 32) {
-#pragma unroll
-                  for (int e = 0; e < 64; ++e)
-                    if (h * 32 + e >= bound) v[e] = neg_inf;
-                }
-                float t0 = v[0], t1 = v[1], t2 = v[2], t3 = v[3];
-#pragma unroll
-                for (int e = 4; e < 64; e += 4) {
-                  t0 = fmaxf(t0, v[e]);
-                  t1 = fmaxf(t1, v[e + 1]);
-                  t2 = fmaxf(t2, v[e + 2]);
-                  t3 = fmaxf(t3, v[e + 3]);
-                }
-                const float nm = fmaxf(run_m[mt], fmaxf(fmaxf(t0, t1), fmaxf(t2, t3)));
-                if (nm != neg_inf) {
-                  float z0 = run_m[mt] == neg_inf ? 0.f : run_z[mt] * fast_exp2(run_m[mt] - nm);
-                  float z1 = 0.f, z2 = 0.f, z3 = 0.f;
-#pragma unroll
-                  for (int e = 0; e < 64; e += 4) {
-                    z0 += fast_exp2(v[e] - nm);
-                    z1 += fast_exp2(v[e + 1] - nm);
-                    z2 += fast_exp2(v[e + 2] - nm);
-                    z3 += fast_exp2(v[e + 3] - nm);
+      // Row chunks of a unit run one after another; chunk ch's rows have their
+      // own lse, and the per-key pooled value is carried across chunks in s_u
+      // (log2 of the max so far, or the sum so far) by the thread that owns the
+      // key, which is the same thread in every chunk (2T tiles per chunk).
+      for (int ch = 0; ch < C && ok; ++ch, ++ci) {
+        const int* limc = lim + ch * lay.rows64;
+        const int Rc = min(R, lay.Rtot - ch * R);  // real rows of this chunk
+        const bool first = ch == 0, last = ch == C - 1;
+        float run_m[2] = {neg_inf, neg_inf}, run_z[2] = {0.f, 0.f};
+        for (int s = 0; s < 2 * T && ok; ++s, ++g) {
+          const int b = (int)(g & 1);
+          if (b == grp) {
+            ok = __all_sync(kFull, mbar_wait(&tfull[b], (uint32_t)((g >> 1) & 1), ctl, P.status));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t col0 = tmem + lane_base + (uint32_t)(b * lay.bufcols);
+            const int kt = s < T ? s : 2 * T - 1 - s;
+            if (s < T) {
+              // pass 1: this thread owns observation row et (and a row of the second M tile)
+              for (int mt = 0; mt < lay.mtiles; ++mt) {
+                const int row = mt ? lay.Rp16 - 128 + et : et;
+                // The second M tile overlaps the first on rows below 128. tcgen05.ld
+                // is warp-collective (.sync.aligned), so only whole warps may skip
+                // it; lanes holding a duplicate row load and discard (bound 0
+                // masks every key, which leaves their running max and sum as is).
+                const bool dup = mt && row < 128;
+                if (__all_sync(kFull, dup)) continue;
+                const int bound = dup ? 0 : limc[row] - kt * kTileKeys;  // keys [0, bound) are visible
+  #pragma unroll
+                for (int h = 0; h < 4; h += 2) {
+                  float v[64];
+                  tmem_ld32(col0 + (uint32_t)(mt * 128 + h * 32), *reinterpret_cast<float(*)[32]>(&v[0]));
+                  tmem_ld32(col0 + (uint32_t)(mt * 128 + h * 32 + 32), *reinterpret_cast<float(*)[32]>(&v[32]));
+                  tmem_wait_ld();
+                  if (bound < (h + 2) * 32) {
+  #pragma unroll
+                    for (int e = 0; e < 64; ++e)
+                      if (h * 32 + e >= bound) v[e] = neg_inf;
                   }
-                  run_z[mt] = (z0 + z1) + (z2 + z3);
-                  run_m[mt] = nm;
-                }
-              }
-            }
-          } else {
-            // pass 2: this thread owns key j of the tile; columns are observation rows
-            const int j = kt * kTileKeys + et;
-            const bool masked_tile = (kt + 1) * kTileKeys > L - P.nr + 1;
-            if (P.pool_mean) {
-              // mean pooling: the weights exp2(l - lse) summed over the rows
-              // (inaccessible and padding rows add 0), divided by R
-              float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-              for (int c = 0; c < lay.Rp16; c += 64) {
-                float v[64];
-                tmem_ld32(col0 + (uint32_t)c, *reinterpret_cast<float(*)[32]>(&v[0]));
-                tmem_ld32(col0 + (uint32_t)c + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
-                tmem_wait_ld();
-                const float4* l4 = reinterpret_cast<const float4*>(lse + c);
-                if (!masked_tile && c + 64 <= R) {
-#pragma unroll
-                  for (int e = 0; e < 64; e += 4) {
-                    const float4 l = l4[e >> 2];
-                    a0 += fast_exp2(v[e] - l.x);
-                    a1 += fast_exp2(v[e + 1] - l.y);
-                    a2 += fast_exp2(v[e + 2] - l.z);
-                    a3 += fast_exp2(v[e + 3] - l.w);
+                  float t0 = v[0], t1 = v[1], t2 = v[2], t3 = v[3];
+  #pragma unroll
+                  for (int e = 4; e < 64; e += 4) {
+                    t0 = fmaxf(t0, v[e]);
+                    t1 = fmaxf(t1, v[e + 1]);
+                    t2 = fmaxf(t2, v[e + 2]);
+                    t3 = fmaxf(t3, v[e + 3]);
                   }
-                } else {
-                  const int4* b4 = reinterpret_cast<const int4*>(lim + c);
-#pragma unroll
-                  for (int e = 0; e < 64; e += 4) {
-                    const float4 l = l4[e >> 2];
-                    const int4 bd = b4[e >> 2];
-                    a0 += j < bd.x ? fast_exp2(v[e] - l.x) : 0.f;
-                    a1 += j < bd.y ? fast_exp2(v[e + 1] - l.y) : 0.f;
-                    a2 += j < bd.z ? fast_exp2(v[e + 2] - l.z) : 0.f;
-                    a3 += j < bd.w ? fast_exp2(v[e + 3] - l.w) : 0.f;
+                  const float nm = fmaxf(run_m[mt], fmaxf(fmaxf(t0, t1), fmaxf(t2, t3)));
+                  if (nm != neg_inf) {
+                    float z0 = run_m[mt] == neg_inf ? 0.f : run_z[mt] * fast_exp2(run_m[mt] - nm);
+                    float z1 = 0.f, z2 = 0.f, z3 = 0.f;
+  #pragma unroll
+                    for (int e = 0; e < 64; e += 4) {
+                      z0 += fast_exp2(v[e] - nm);
+                      z1 += fast_exp2(v[e + 1] - nm);
+                      z2 += fast_exp2(v[e + 2] - nm);
+                      z3 += fast_exp2(v[e + 3] - nm);
+                    }
+                    run_z[mt] = (z0 + z1) + (z2 + z3);
+                    run_m[mt] = nm;
                   }
                 }
               }
-              if (j < L) s_u[j] = ((a0 + a1) + (a2 + a3)) * inv_rows;
             } else {
-              float m0 = neg_inf, m1 = neg_inf, m2 = neg_inf, m3 = neg_inf;
-              for (int c = 0; c < lay.Rp16; c += 64) {
-                float v[64];
-                tmem_ld32(col0 + (uint32_t)c, *reinterpret_cast<float(*)[32]>(&v[0]));
-                tmem_ld32(col0 + (uint32_t)c + 32, *reinterpret_cast<float(*)[32]>(&v[32]));  // inside the buffer
-                tmem_wait_ld();
-                if (!masked_tile && c + 64 <= R) {
+              // pass 2: this thread owns key j of the tile; columns are observation rows
+              const int j = kt * kTileKeys + et;
+              const bool masked_tile = (kt + 1) * kTileKeys > L - P.nr + 1;
+              if (P.pool_mean) {
+                // mean pooling: the weights exp2(l - lse) summed over the rows
+                // (inaccessible and padding rows add 0), divided by the row count
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                for (int c = 0; c < lay.Rp16; c += 64) {
+                  float v[64];
+                  tmem_ld32(col0 + (uint32_t)c, *reinterpret_cast<float(*)[32]>(&v[0]));
+                  tmem_ld32(col0 + (uint32_t)c + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+                  tmem_wait_ld();
                   const float4* l4 = reinterpret_cast<const float4*>(lse + c);
+                  if (!masked_tile && c + 64 <= Rc) {
   #pragma unroll
-                  for (int e = 0; e < 64; e += 4) {
-                    const float4 l = l4[e >> 2];
-                    m0 = fmaxf(m0, v[e] - l.x);
-                    m1 = fmaxf(m1, v[e + 1] - l.y);
-                    m2 = fmaxf(m2, v[e + 2] - l.z);
-                    m3 = fmaxf(m3, v[e + 3] - l.w);
-                  }
-                } else {
-                  // rows r >= R carry lim = 0, so the visibility test masks them too
-                  const float4* l4 = reinterpret_cast<const float4*>(lse + c);
-                  const int4* b4 = reinterpret_cast<const int4*>(lim + c);
+                    for (int e = 0; e < 64; e += 4) {
+                      const float4 l = l4[e >> 2];
+                      a0 += fast_exp2(v[e] - l.x);
+                      a1 += fast_exp2(v[e + 1] - l.y);
+                      a2 += fast_exp2(v[e + 2] - l.z);
+                      a3 += fast_exp2(v[e + 3] - l.w);
+                    }
+                  } else {
+                    const int4* b4 = reinterpret_cast<const int4*>(limc + c);
   #pragma unroll
-                  for (int e = 0; e < 64; e += 4) {
-                    const float4 l = l4[e >> 2];
-                    const int4 bd = b4[e >> 2];
-                    m0 = fmaxf(m0, j < bd.x ? v[e] - l.x : neg_inf);
-                    m1 = fmaxf(m1, j < bd.y ? v[e + 1] - l.y : neg_inf);
-                    m2 = fmaxf(m2, j < bd.z ? v[e + 2] - l.z : neg_inf);
-                    m3 = fmaxf(m3, j < bd.w ? v[e + 3] - l.w : neg_inf);
+                    for (int e = 0; e < 64; e += 4) {
+                      const float4 l = l4[e >> 2];
+                      const int4 bd = b4[e >> 2];
+                      a0 += j < bd.x ? fast_exp2(v[e] - l.x) : 0.f;
+                      a1 += j < bd.y ? fast_exp2(v[e + 1] - l.y) : 0.f;
+                      a2 += j < bd.z ? fast_exp2(v[e + 2] - l.z) : 0.f;
+                      a3 += j < bd.w ? fast_exp2(v[e + 3] - l.w) : 0.f;
+                    }
                   }
                 }
+                if (j < L) {
+                  const float a = ((a0 + a1) + (a2 + a3)) + (first ? 0.f : s_u[j]);
+                  s_u[j] = last ? a * inv_rows : a;
+                }
+              } else {
+                float m0 = neg_inf, m1 = neg_inf, m2 = neg_inf, m3 = neg_inf;
+                for (int c = 0; c < lay.Rp16; c += 64) {
+                  float v[64];
+                  tmem_ld32(col0 + (uint32_t)c, *reinterpret_cast<float(*)[32]>(&v[0]));
+                  tmem_ld32(col0 + (uint32_t)c + 32, *reinterpret_cast<float(*)[32]>(&v[32]));  // inside the buffer
+                  tmem_wait_ld();
+                  if (!masked_tile && c + 64 <= Rc) {
+                    const float4* l4 = reinterpret_cast<const float4*>(lse + c);
+    #pragma unroll
+                    for (int e = 0; e < 64; e += 4) {
+                      const float4 l = l4[e >> 2];
+                      m0 = fmaxf(m0, v[e] - l.x);
+                      m1 = fmaxf(m1, v[e + 1] - l.y);
+                      m2 = fmaxf(m2, v[e + 2] - l.z);
+                      m3 = fmaxf(m3, v[e + 3] - l.w);
+                    }
+                  } else {
+                    // padding rows carry lim = 0, so the visibility test masks them too
+                    const float4* l4 = reinterpret_cast<const float4*>(lse + c);
+                    const int4* b4 = reinterpret_cast<const int4*>(limc + c);
+    #pragma unroll
+                    for (int e = 0; e < 64; e += 4) {
+                      const float4 l = l4[e >> 2];
+                      const int4 bd = b4[e >> 2];
+                      m0 = fmaxf(m0, j < bd.x ? v[e] - l.x : neg_inf);
+                      m1 = fmaxf(m1, j < bd.y ? v[e + 1] - l.y : neg_inf);
+                      m2 = fmaxf(m2, j < bd.z ? v[e + 2] - l.z : neg_inf);
+                      m3 = fmaxf(m3, j < bd.w ? v[e + 3] - l.w : neg_inf);
+                    }
+                  }
+                }
+                float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+                if (j < L) {
+                  if (!first) mx = fmaxf(mx, s_u[j]);
+                  s_u[j] = !last ? mx : (mx == neg_inf ? 0.f : fast_exp2(mx));
+                }
               }
-              const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-              if (j < L) s_u[j] = mx == neg_inf ? 0.f : fast_exp2(mx);
             }
+            tc_fence_before();
+            mbar_arrive(&tempty[b]);
           }
-          tc_fence_before();
-          mbar_arrive(&tempty[b]);
-        }
-        if (s == T - 1) {
-          // merge the two groups' row statistics into lse
-          for (int mt = 0; mt < lay.mtiles; ++mt) {
-            const int row = mt ? lay.Rp16 - 128 + et : et;
-            if (mt && row < 128) continue;
-            pm[grp * lay.qrows + row] = run_m[mt];
-            pz[grp * lay.qrows + row] = run_z[mt];
-          }
-          mbar_arrive(lsebar);
-          ok = __all_sync(kFull, mbar_wait(lsebar, (uint32_t)(it & 1), ctl, P.status));
-          if (!ok) break;
-          if (grp == 0) {
+          if (s == T - 1) {
+            // merge the two groups' row statistics into lse
             for (int mt = 0; mt < lay.mtiles; ++mt) {
               const int row = mt ? lay.Rp16 - 128 + et : et;
               if (mt && row < 128) continue;
-              const float ma = pm[row], mb = pm[lay.qrows + row];
-              const float mm = fmaxf(ma, mb);
-              float zz = 0.f;
-              if (mm != neg_inf)
-                zz = (ma == neg_inf ? 0.f : pz[row] * fast_exp2(ma - mm)) +
-                     (mb == neg_inf ? 0.f : pz[lay.qrows + row] * fast_exp2(mb - mm));
-              lse[row] = zz > 0.f ? mm + fast_log2(zz) : neg_inf;
+              pm[grp * lay.qrows + row] = run_m[mt];
+              pz[grp * lay.qrows + row] = run_z[mt];
             }
+            mbar_arrive(lsebar);
+            ok = __all_sync(kFull, mbar_wait(lsebar, (uint32_t)(ci & 1), ctl, P.status));
+            if (!ok) break;
+            if (grp == 0) {
+              for (int mt = 0; mt < lay.mtiles; ++mt) {
+                const int row = mt ? lay.Rp16 - 128 + et : et;
+                if (mt && row < 128) continue;
+                const float ma = pm[row], mb = pm[lay.qrows + row];
+                const float mm = fmaxf(ma, mb);
+                float zz = 0.f;
+                if (mm != neg_inf)
+                  zz = (ma == neg_inf ? 0.f : pz[row] * fast_exp2(ma - mm)) +
+                       (mb == neg_inf ? 0.f : pz[lay.qrows + row] * fast_exp2(mb - mm));
+                lse[row] = zz > 0.f ? mm + fast_log2(zz) : neg_inf;
+              }
+            }
+            mbar_arrive(lse2bar);
+            ok = __all_sync(kFull, mbar_wait(lse2bar, (uint32_t)(ci & 1), ctl, P.status));
+            // this unit's scores go to sc[b_sc]: the selector must be done with unit it - NSC
+            if (ok && first && it >= NSC)
+              ok = __all_sync(kFull, mbar_wait(&sfree[b_sc], (uint32_t)(((it / NSC) + 1) & 1), ctl, P.status));
+            if (!ok) break;
           }
-          mbar_arrive(lse2bar);
-          ok = __all_sync(kFull, mbar_wait(lse2bar, (uint32_t)(it & 1), ctl, P.status));
-          // this unit's scores go to sc[b_sc]: the selector must be done with unit it - NSC
-          if (ok && it >= NSC)
-            ok = __all_sync(kFull, mbar_wait(&sfree[b_sc], (uint32_t)(((it / NSC) + 1) & 1), ctl, P.status));
-          if (!ok) break;
+          if (last && s == 2 * T - 1) mbar_arrive(&sready[b_sc]);
         }
-        if (s == 2 * T - 1) mbar_arrive(&sready[b_sc]);
-      }
-      // rows of the next unit: the MMAs of this one must be done with the buffers
-      if (ok && it + 1 < mine) {
-        ok = __all_sync(kFull, mbar_wait(qfree, (uint32_t)(it & 1), ctl, P.status));
-        if (ok) build_rows(it + 1, bt, 2 * kEpiThreads);
+        // rows of the next chunk: the MMAs of this one must be done with the buffers
+        if (ok && (it + 1 < mine || !last)) {
+          ok = __all_sync(kFull, mbar_wait(qfree, (uint32_t)(ci & 1), ctl, P.status));
+          if (ok) build_rows(last ? it + 1 : it, last ? 0 : ch + 1, bt, 2 * kEpiThreads);
+        }
       }
     }
   }

@@ -174,6 +174,30 @@ def test_order_free_needs_recent_window_inside_the_tail():
         bkv.bkv_destroy(h)
 
 
+# ---------------------------------------------------------------------------- row chunks
+
+@pytest.mark.parametrize("name,over", [
+    # G x (16 beacons + 16 recents) observation rows per unit
+    ("gqa12_384_rows", dict(heads=12, kv_heads=1)),        # 2 chunks of 192
+    ("gqa16_512_rows", dict(heads=16, kv_heads=1)),        # 2 chunks of 256
+    ("gqa20_640_rows", dict(heads=20, kv_heads=1)),        # 3 chunks: 214, 214, 212
+    ("gqa9_two_kv_288_rows", dict(heads=18, kv_heads=2)),  # 2 chunks of 144
+])
+@pytest.mark.parametrize("pool", ["max", "mean"])
+def test_row_chunks_tiny(name, over, pool):
+    """Units with more than 256 observation rows are scored chunk by chunk:
+    per-chunk log-sum-exp, then the pooled value carried across chunks."""
+    w = TINY.with_(**{"steps": 240, **over})
+    rep = run_lockstep(w, seed=0xBEAE0 + len(name), pool=pool)
+    assert_clean(rep, min_evictions=3)
+
+
+def test_row_chunks_order_free_many_tiles():
+    w = TINY.with_(heads=12, kv_heads=1, budget=700, steps=800)
+    rep = run_lockstep(w, seed=0xBEAE8, order_free=True)
+    assert_clean(rep, min_evictions=3)
+
+
 # ---------------------------------------------------------------------------- the pages' variants
 
 @pytest.mark.parametrize("name,over", [
@@ -293,10 +317,17 @@ def test_prefill_long_prompt_then_large_eviction():
 def test_prefill_gqa7_wide_exponents():
     # 96 prompt steps keep the FPS phase of a plain stream: at each eviction a
     # head holds 16 beacons + 16 recents, so 7 heads make 224 observation rows
-    # (a prompt of 90 would leave 22 + 16 per head, 266 rows: beyond the 256
-    # the score kernel takes)
     w = TINY.with_(heads=7, kv_heads=1, steps=260)
     rep = run_lockstep(w, seed=0xBEAD4, prefill=96, query_hook=wide_queries)
+    assert_clean(rep, min_evictions=3)
+
+
+@pytest.mark.parametrize("pool", ["max", "mean"])
+def test_prefill_gqa7_off_phase_266_rows(pool):
+    # a prompt of 90 leaves 22 beacons + 16 recents per head at the first
+    # evictions: 7 x 38 = 266 observation rows, scored in two chunks of 133
+    w = TINY.with_(heads=7, kv_heads=1, steps=260)
+    rep = run_lockstep(w, seed=0xBEAD6, prefill=90, pool=pool)
     assert_clean(rep, min_evictions=3)
 
 
