@@ -38,6 +38,11 @@
 //            TMEM -> registers, online log-sum-exp in pass 1, max-pooling in
 //            pass 2, scores to shared memory; between units they build the
 //            next unit's rotated rows (the tensor cores wait for them).
+// L2 policies: pass-1 loads keep their lines (evict_last) so that pass 2
+// finds them in L2, and pass 2 walks the tiles in reverse, newest first: when
+// a unit's tiles do not all stay in L2, the ones pass 1 read last are the ones
+// still there. Every compaction copy marks its lines evict_first.
+//
 // Every cross-warp wait is a bounded wait on an mbarrier; on expiry the kernel
 // latches BKV_ERR_TIMEOUT, every role stops at its next wait, outstanding
 // copies are drained and the TMEM is freed before the CTA exits.
@@ -48,234 +53,11 @@
 // order like the values: each lane keeps a sorted list of its smallest
 // (score bits, ~slot) keys, the warp extracts the D smallest from the list
 // heads, and a ballot scan writes the kept (and dropped) slots in order.
-#include "bkv_internal.cuh"
+#include "score_common.cuh"
 
 namespace bkv {
 
 namespace {
-
-constexpr int kThreads = 384;
-constexpr int kTileKeys = 128;
-constexpr int kSlabBytes = kTileKeys * 128;   // 128 rows x 64 bf16: one SWIZZLE_128B box
-constexpr int kTileBytes = 2 * kSlabBytes;    // 32 KB per 128-key tile
-constexpr int kEpiThreads = 128;              // one epilogue warpgroup (warps 4-7 or 8-11)
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr long long kWaitCycles = 2000000000LL;  // ~1 s: far beyond any legitimate wait
-constexpr unsigned kFull = 0xFFFFFFFFu;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-// ------------------------------------------------------------------ mbarrier
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-struct Ctl {
-  volatile int abort;  // raised by the first role whose wait ran out
-  uint32_t tmem_base;
-};
-
-// Bounded wait for the phase with the given parity. Returns false (after
-// latching the timeout and raising the abort flag) if it never completes, or
-// as soon as another role has aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Ctl* ctl, uint32_t* status) {
-  if (mbar_test(b, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_test(b, parity)) {
-    if (ctl->abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
-      latch(status, BKV_ERR_TIMEOUT);
-      ctl->abort = 1;
-      return false;
-    }
-  }
-  return true;
-}
-
-// ------------------------------------------------------------------ L2 policies
-// K tiles are read twice (pass 1, then pass 2 once every row's log-sum-exp is
-// known); the compaction streams rows it touches once. Pass-1 loads keep their
-// lines (evict_last) so that pass 2 finds them in L2, and pass 2 walks the
-// tiles in reverse, newest first: when a unit's tiles do not all stay in L2,
-// the ones pass 1 read last are the ones still there. Every compaction copy
-// marks its lines evict_first.
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_normal() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-// ------------------------------------------------------------------ TMA
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
-// Non-tensor bulk copies: global -> shared with an mbarrier, shared -> global
-// in bulk groups.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                          uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
-      ::"r"(dst), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes, uint64_t policy) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
-               ::"l"(dst), "r"(src), "r"(bytes), "l"(policy)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// ------------------------------------------------------------------ tcgen05
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
-               "r"(ncols));
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
-// 32 TMEM lanes x 32 consecutive 32-bit columns: thread t of the warp reads
-// lane (lane base of its warp quarter) + t into 32 registers.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t* r = reinterpret_cast<uint32_t*>(v);
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor for a K-major operand in the canonical
-// SWIZZLE_128B layout: 8-row groups of 128-byte rows, 1024 bytes apart (SBO);
-// descriptor version 1; layout type 2 = SWIZZLE_128B. Moving along K inside
-// the 128-byte swizzle atom advances the start address by 32 bytes per 16
-// bf16 elements.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float fast_log2(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Keep set of one unit from its scores sc[0, L). One warp. The D = L - budget
-// dropped slots are the D smallest 64-bit keys (score bits << 32 | ~slot)
-// among the candidates [prefix, L - recent): lower score first, and among
-// equal scores the higher slot first, so the lower slot wins a tie (scores
-// are >= 0, so their bit patterns order like the values). Each lane keeps the
-// kList smallest keys of its own candidates, built without data-dependent
-// branches: batches of 8 keys are sorted by Batcher's odd-even network and
-// merged into the list by a bitonic half-cleaner. The warp then extracts the
-// global minimum D times; a lane whose list runs dry rebuilds it from the
-// keys above the last one it gave up. dropped[] is a bitmask over slots;
-// drops[] receives the dropped slots ascending. out[] receives the kept
-// slots ascending, or with order_free the layout of the order-free
-// compaction. Returns true if a score was NaN.
-constexpr int kList = 8;
-typedef unsigned long long u64;
-constexpr u64 kNoKey = ~0ull;
-
-__device__ __forceinline__ void cswap(u64& a, u64& b) {
-  const u64 lo = a < b ? a : b, hi = a < b ? b : a;
-  a = lo;
-  b = hi;
-}
-__device__ __forceinline__ void sort8(u64 (&k)[8]) {
-  cswap(k[0], k[1]); cswap(k[2], k[3]); cswap(k[4], k[5]); cswap(k[6], k[7]);
-  cswap(k[0], k[2]); cswap(k[1], k[3]); cswap(k[4], k[6]); cswap(k[5], k[7]);
-  cswap(k[1], k[2]); cswap(k[5], k[6]);
-  cswap(k[0], k[4]); cswap(k[1], k[5]); cswap(k[2], k[6]); cswap(k[3], k[7]);
-  cswap(k[2], k[4]); cswap(k[3], k[5]);
-  cswap(k[1], k[2]); cswap(k[3], k[4]); cswap(k[5], k[6]);
-}
-// list <- the 8 smallest of list and k, both sorted ascending
-__device__ __forceinline__ void merge8(u64 (&list)[8], const u64 (&k)[8]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) list[i] = list[i] < k[7 - i] ? list[i] : k[7 - i];  // bitonic
-#pragma unroll
-  for (int dd = 4; dd > 0; dd >>= 1)
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if ((i & dd) == 0) cswap(list[i], list[i + dd]);
-}
 
 // Large drop counts (D > kRadixFrom): the D-th smallest score is found digit
 // by digit (four 8-bit radix passes over a 256-bin shared histogram of the
@@ -399,6 +181,19 @@ __device__ bool list_drop(const float* sc, int c0, int c1, int D, uint32_t* drop
   return __any_sync(kFull, bad);
 }
 
+// Keep set of one unit from its scores sc[0, L). One warp. The D = L - budget
+// dropped slots are the D smallest 64-bit keys (score bits << 32 | ~slot)
+// among the candidates [prefix, L - recent): lower score first, and among
+// equal scores the higher slot first, so the lower slot wins a tie (scores
+// are >= 0, so their bit patterns order like the values). Each lane keeps the
+// kList smallest keys of its own candidates, built without data-dependent
+// branches: batches of 8 keys are sorted by Batcher's odd-even network and
+// merged into the list by a bitonic half-cleaner. The warp then extracts the
+// global minimum D times; a lane whose list runs dry rebuilds it from the
+// keys above the last one it gave up. dropped[] is a bitmask over slots;
+// drops[] receives the dropped slots ascending. out[] receives the kept
+// slots ascending, or with order_free the layout of the order-free
+// compaction. Returns true if a score was NaN.
 __device__ bool select_keep(const float* sc, int L, int prefix, int recent, int budget, int32_t* out,
                             uint32_t* dropped, int* drops, bool order_free, int* hist) {
   static_assert(kList == 8, "the list networks are written for 8 keys");
@@ -543,12 +338,6 @@ __host__ __device__ inline Layout make_layout(int Rtot, int L, int nr, int budge
   return s;
 }
 
-__device__ __forceinline__ void unit_geom(int u, int batch, int kv_heads, int& layer, int& seq, int& kvh) {
-  kvh = u % kv_heads;
-  seq = (u / kv_heads) % batch;
-  layer = u / (kv_heads * batch);
-}
-
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_constant__ ScoreParams P) {
@@ -615,31 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   // zero both row buffers once: padding rows stay zero for the whole launch
   for (int i = tid; i < (int)(2 * (lay.q_lo - lay.q_hi) / 16); i += kThreads)
     reinterpret_cast<uint4*>(q_hi)[i] = make_uint4(0, 0, 0, 0);
-  // per-launch tables, chunk by chunk: the key bound of each row (0 masks
-  // padding rows) and each row's source (x = -1: a zero padding row)
-  for (int i = tid; i < lay.chunks * lay.rows64; i += kThreads) {
-    const int rl = i % lay.rows64, r = (i / lay.rows64) * R + rl;
-    int bound = 0;
-    if (rl < R && r < lay.Rtot) {
-      const int w = r % per_head;
-      bound = w < P.nb ? L : L - P.nr + (w - P.nb) + 1;
-    }
-    lim[i] = bound;
-  }
-  for (int i = tid; i < lay.chunks * lay.qrows; i += kThreads) {
-    const int rl = i % lay.qrows, r = (i / lay.qrows) * R + rl;
-    if (rl >= R || r >= lay.Rtot) {
-      rowinfo[i] = make_int2(-1, 0);
-      continue;
-    }
-    const int gi = r / per_head, w = r % per_head;
-    if (w < P.nb) {
-      rowinfo[i] = make_int2((gi * P.fps_cap + w) * 16, 0);
-    } else {
-      const int kq = w - P.nb;
-      rowinfo[i] = make_int2(((gi * P.n_rq + (P.ring_first + kq) % P.n_rq) * 16) | (1 << 30), 1 + kq);
-    }
-  }
+  // per-launch tables, chunk by chunk: the key bound and the source of each row
+  for (int c = 0; c < lay.chunks; ++c)
+    fill_row_tables(lim + c * lay.rows64, rowinfo + c * lay.qrows, c * R, R, lay.Rtot, lay.rows64, lay.qrows,
+                    P.nb, P.nr, L, P.fps_cap, P.n_rq, P.ring_first, tid, kThreads);
   const uint32_t ncols = 2 * (uint32_t)lay.bufcols;
   if (warp == 1) tmem_alloc(&ctl->tmem_base, ncols);
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -656,70 +424,18 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
     unit_geom(blockIdx.x + it * gridDim.x, P.batch, P.kv_heads, layer, seq, kvh);
     return ((int64_t)layer * P.batch + seq) * (P.kv_heads * P.group) + (int64_t)kvh * P.group;
   };
-  // source of row r of chunk c (nullptr: zero padding) and its RoPE table row
-  auto row_src = [&](int64_t head0, int c, int r, int& prow) -> const uint4* {
+  // source of row r of chunk c (nullptr: zero padding)
+  auto row_src = [&](int64_t head0, int c, int r) -> const uint4* {
     const int2 info = rowinfo[c * lay.qrows + r];
-    prow = info.y;
     if (info.x < 0) return nullptr;
     const uint4* base = (info.x & (1 << 30)) ? P.rq + head0 * P.n_rq * 16 : P.bq + head0 * P.fps_cap * 16;
     return base + (info.x & ~(1 << 30));
   };
-  // Rotated observation rows of chunk c of unit `it`, split into bf16 hi + lo,
-  // written in the SWIZZLE_128B K-major layout; thread t of n builds items
-  // t, t + n, ...
+  // rotated observation rows of chunk c of unit `it`; thread t of n
   auto build_rows = [&](int it, int c, int t, int n) {
-    constexpr int kBatch = 4;  // items per thread with loads in flight together
     const int64_t head0 = head_base(it);
-    for (int base = 0; base < R * 8; base += n * kBatch) {
-      uint4 xl[kBatch], xh[kBatch];
-      int prow[kBatch];
-#pragma unroll
-      for (int bi = 0; bi < kBatch; ++bi) {
-        const int idx = base + t + n * bi;
-        xl[bi] = xh[bi] = make_uint4(0, 0, 0, 0);
-        prow[bi] = 0;
-        if (idx < R * 8) {
-          const uint4* src = row_src(head0, c, idx >> 3, prow[bi]);
-          if (src) {
-            xl[bi] = src[idx & 7];
-            xh[bi] = src[(idx & 7) + 8];
-          }
-        }
-      }
-#pragma unroll
-      for (int bi = 0; bi < kBatch; ++bi) {
-        const int idx = base + t + n * bi;
-        if (idx >= R * 8) break;
-        const int r = idx >> 3, part = idx & 7;
-        const __nv_bfloat162* l2 = reinterpret_cast<const __nv_bfloat162*>(&xl[bi]);
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&xh[bi]);
-        uint4 o[4];  // slab 0 hi, slab 1 hi, slab 0 lo, slab 1 lo
-        __nv_bfloat162* o0 = reinterpret_cast<__nv_bfloat162*>(&o[0]);
-        __nv_bfloat162* o1 = reinterpret_cast<__nv_bfloat162*>(&o[1]);
-        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o[2]);
-        __nv_bfloat162* o3 = reinterpret_cast<__nv_bfloat162*>(&o[3]);
-        const float2* cs = P.rope + prow[bi] * kRopePairs + part * 8;  // shared by all units: L1-resident
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 a = __bfloat1622float2(l2[e]), bb = __bfloat1622float2(h2[e]);
-          const float2 c0 = __ldg(cs + 2 * e), c1 = __ldg(cs + 2 * e + 1);
-          const float2 vl =
-              make_float2((a.x * c0.x - bb.x * c0.y) * qk_scale, (a.y * c1.x - bb.y * c1.y) * qk_scale);
-          const float2 vh =
-              make_float2((bb.x * c0.x + a.x * c0.y) * qk_scale, (bb.y * c1.x + a.y * c1.y) * qk_scale);
-          o0[e] = __float22bfloat162_rn(vl);
-          o1[e] = __float22bfloat162_rn(vh);
-          const float2 fl = __bfloat1622float2(o0[e]), fh = __bfloat1622float2(o1[e]);
-          o2[e] = __floats2bfloat162_rn(vl.x - fl.x, vl.y - fl.y);
-          o3[e] = __floats2bfloat162_rn(vh.x - fh.x, vh.y - fh.y);
-        }
-        const uint32_t inrow = (uint32_t)r * 128 + (uint32_t)((part ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(q_hi + inrow) = o[0];
-        *reinterpret_cast<uint4*>(q_hi + slab_q + inrow) = o[1];
-        *reinterpret_cast<uint4*>(q_lo + inrow) = o[2];
-        *reinterpret_cast<uint4*>(q_lo + slab_q + inrow) = o[3];
-      }
-    }
+    build_obs_rows(q_hi, q_lo, slab_q, R, rowinfo + c * lay.qrows, P.bq + head0 * P.fps_cap * 16,
+                   P.rq + head0 * P.n_rq * 16, P.rope, qk_scale, t, n);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive(qready);
   };
@@ -1010,8 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
         if (!ok) break;
         const int64_t h1 = head_base((ci + 1) / lay.chunks);
         for (int r = lane; r < R; r += 32) {
-          int pr;
-          const char* src = reinterpret_cast<const char*>(row_src(h1, (ci + 1) % lay.chunks, r, pr));
+          const char* src = reinterpret_cast<const char*>(row_src(h1, (ci + 1) % lay.chunks, r));
           if (!src) continue;
           asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
           asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128));
