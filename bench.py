@@ -483,7 +483,11 @@ def run_ours(args, w):
 def run_e2e(args, w, bkv, h, K, V, kept, kptr, vptr, qpool, state, dev, cs):
     """Same step through the C ABI, with each step's inputs coming from pinned
     host memory (the period's queries and the new K/V rows) and the keep sets
-    going back to the host, all inside the timed region."""
+    going back to the host, all inside the timed region. The copies run on a
+    second stream, double-buffered, so that step k + 1's inputs travel while
+    step k's eviction runs: inputs land in device staging buffers, and the new
+    K/V rows move into the cache (a device copy) once the eviction that reads
+    those slots is done."""
     import torch
     q_host = qpool.cpu().pin_memory()  # one period of queries per step, host side
     tail = torch.empty(w.layers, 2, w.batch, w.kv_heads, w.period, w.d, dtype=torch.bfloat16)
@@ -491,49 +495,90 @@ def run_e2e(args, w, bkv, h, K, V, kept, kptr, vptr, qpool, state, dev, cs):
         tail[l, 0] = K[l][:, :, w.budget:w.max_cache].cpu()
         tail[l, 1] = V[l][:, :, w.budget:w.max_cache].cpu()
     tail = tail.pin_memory()
-    kept_host = torch.empty(kept.shape, dtype=kept.dtype).pin_memory()
-    qdev = torch.empty_like(qpool[0])
-    n_periods = qpool.shape[0]
+    n_periods = q_host.shape[0]
+    xs = torch.cuda.Stream(dev)
+    qstage = [torch.empty_like(qpool[0]) for _ in range(2)]
+    tstage = [torch.empty(tail.shape, dtype=tail.dtype, device=dev) for _ in range(2)]
+    kept_dev = [kept, torch.empty_like(kept)]
+    kept_host = [torch.empty(kept.shape, dtype=kept.dtype).pin_memory() for _ in range(2)]
+    ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("staged", "used", "evicted", "read")}
 
-    def step():
+    def stage(k):
+        """Copy stream: step k's queries and new K/V rows into staging buffer k % 2."""
+        b = k % 2
+        with torch.cuda.stream(xs):
+            if k >= 2:
+                xs.wait_event(ev["used"][b])  # step k - 2 is done with this buffer
+            qstage[b].copy_(q_host[k % n_periods], non_blocking=True)
+            tstage[b].copy_(tail, non_blocking=True)
+            ev["staged"][b].record(xs)
+
+    def step(k):
+        b = k % 2
         t = state["t"]
-        bkv.bkv_evict_ptrs(h, kptr, vptr, w.max_cache, t, kept.data_ptr())
-        kept_host.copy_(kept, non_blocking=True)
-        qdev.copy_(q_host[state["e"] % n_periods], non_blocking=True)
+        if k >= 2:
+            cs.wait_event(ev["read"][b])  # step k - 2's keep sets have reached the host
+        bkv.bkv_evict_ptrs(h, kptr, vptr, w.max_cache, t, kept_dev[b].data_ptr())
+        ev["evicted"][b].record(cs)
+        with torch.cuda.stream(xs):
+            xs.wait_event(ev["evicted"][b])
+            kept_host[b].copy_(kept_dev[b], non_blocking=True)
+            ev["read"][b].record(xs)
+        cs.wait_event(ev["staged"][b])
         for l in range(w.layers):
-            K[l][:, :, w.budget:w.max_cache].copy_(tail[l, 0], non_blocking=True)
-            V[l][:, :, w.budget:w.max_cache].copy_(tail[l, 1], non_blocking=True)
+            K[l][:, :, w.budget:w.max_cache].copy_(tstage[b][l, 0], non_blocking=True)
+            V[l][:, :, w.budget:w.max_cache].copy_(tstage[b][l, 1], non_blocking=True)
         for i in range(w.period):
-            bkv.bkv_append_queries(h, qdev[i], t + 1 + i)
+            bkv.bkv_append_queries(h, qstage[b][i], t + 1 + i)
+        ev["used"][b].record(cs)
         state["t"] = t + w.period
-        state["e"] += 1
 
-    state["e"] = 0
-    for _ in range(max(1, args.warmup)):
-        step()
+    total = max(1, args.warmup) + args.steps
+    stage(0)
+    stage(1)
+    for k in range(max(1, args.warmup)):
+        step(k)
+        if k + 2 < total:
+            stage(k + 2)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(cs)
-    for _ in range(args.steps):
-        step()
+    for k in range(max(1, args.warmup), total):
+        step(k)
+        if k + 2 < total:
+            stage(k + 2)
+    cs.wait_event(ev["read"][(total - 1) % 2])  # the last keep sets are on the host
     e1.record(cs)
     torch.cuda.synchronize(dev)
     bkv.bkv_sync(h)
     return {"elapsed_ms": e0.elapsed_time(e1), "steps": args.steps,
-            "h2d": qdev.numel() * 2 + tail.numel() * 2, "d2h": kept_host.numel() * 4}
+            "h2d": qstage[0].numel() * 2 + tail.numel() * 2, "d2h": kept_host[0].numel() * 4}
+
+
+def kernel_source_digest(kernel: str):
+    """SHA-256 prefix of a kernel's source file followed by every csrc/*.cuh
+    (sorted): any change to the kernel or a header it may include changes it."""
+    import glob
+    import hashlib
+    src = {"score_select": "k_score.cu", "fps": "k_fps.cu",
+           "append": "k_append.cu", "rope": "k_append.cu"}.get(kernel)
+    if not src:
+        return None
+    csrc = os.path.join(ROOT, "kv_cache_eviction_head_gb300", "csrc")
+    h = hashlib.sha256()
+    for p in [os.path.join(csrc, src)] + sorted(glob.glob(os.path.join(csrc, "*.cuh"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def read_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it matches the
-    current kernel source (profiles/traffic.md lists the source hash)."""
-    import hashlib
+    current kernel source (profiles/traffic.md lists the source digest)."""
     path = os.path.join(ROOT, "profiles", "traffic.md")
-    src = {"score_select": "k_score.cu", "fps": "k_fps.cu",
-           "append": "k_append.cu", "rope": "k_append.cu"}.get(kernel)
-    if not src or not os.path.exists(path):
+    digest = kernel_source_digest(kernel)
+    if not digest or not os.path.exists(path):
         return None
-    with open(os.path.join(ROOT, "kv_cache_eviction_head_gb300", "csrc", src), "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()[:16]
     with open(path) as f:
         for line in f:
             cells = [c.strip() for c in line.strip().strip("|").split("|")]
