@@ -33,6 +33,7 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
+constexpr int kBatch = 8;  // candidates per warp whose row loads are in flight together
 constexpr float kCosErr = 2e-5f;
 constexpr float kMeanErr = 2.5e-5f;
 constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -158,9 +159,17 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
     return;
   }
 
-  // lane's four components of candidate j as float32, scaled by 2^(127 - E_j)
-  auto load4 = [&](int j, float (&y)[4], uint32_t& emax) {
-    const uint2 w = __ldg(reinterpret_cast<const uint2*>(row(j)) + lane);
+  // The lane's 8 bytes (four components) of the rows of candidates j0,
+  // j0 + kWarps, ..., issued together: one memory latency per batch.
+  auto fetch = [&](int j0, uint2 (&w)[kBatch]) {
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int j = j0 + b * kWarps;
+      w[b] = j < N ? __ldg(reinterpret_cast<const uint2*>(row(j)) + lane) : make_uint2(0u, 0u);
+    }
+  };
+  // lane's four components of a row as float32 (the bf16 values), and their largest biased exponent
+  auto split4 = [&](uint2 w, float (&y)[4], uint32_t& emax) {
     const uint32_t h[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
     emax = 0;
 #pragma unroll
@@ -169,10 +178,11 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
       y[i] = __uint_as_float(h[i] << 16);
     }
   };
-  auto unit4 = [&](int j, float (&u)[4]) {
+  // unit vector components of candidate j from its fetched bytes
+  auto unit4 = [&](int j, uint2 w, float (&u)[4]) {
     float y[4];
     uint32_t e;
-    load4(j, y, e);
+    split4(w, y, e);
     const float scale = __int_as_float(max(254 - (int)sm.E[j], 1) << 23);
     const float iv = sm.inv[j];
 #pragma unroll
@@ -182,28 +192,35 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
   // ---- phase A: scaling, norms, flags, sum of unit vectors
   double macc[4] = {0.0, 0.0, 0.0, 0.0};
   bool bad = false;
-  for (int j = warp; j < N; j += kWarps) {
-    float y[4];
-    uint32_t e;
-    load4(j, y, e);
+  for (int j0 = warp; j0 < N; j0 += kWarps * kBatch) {
+    uint2 wb[kBatch];
+    fetch(j0, wb);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) e = max(e, __shfl_xor_sync(kFull, e, off));
-    bad |= e == 0xFFu;
-    const float scale = __int_as_float(max(254 - (int)e, 1) << 23);
+    for (int b = 0; b < kBatch; ++b) {
+      const int j = j0 + b * kWarps;
+      if (j >= N) break;  // uniform across the warp
+      float y[4];
+      uint32_t e;
+      split4(wb[b], y, e);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) y[i] = __fmul_rn(y[i], scale);
-    float n2 = __fmul_rn(y[0], y[0]);
-    n2 = __fmaf_rn(y[1], y[1], n2);
-    n2 = __fmaf_rn(y[2], y[2], n2);
-    n2 = __fmaf_rn(y[3], y[3], n2);
-    n2 = warp_sum(n2);
-    const float iv = n2 > 0.f ? rsqrtf(n2) : 0.f;
+      for (int off = 16; off > 0; off >>= 1) e = max(e, __shfl_xor_sync(kFull, e, off));
+      bad |= e == 0xFFu;
+      const float scale = __int_as_float(max(254 - (int)e, 1) << 23);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) macc[i] = __dadd_rn(macc[i], (double)__fmul_rn(y[i], iv));
-    if (lane == 0) {
-      sm.inv[j] = iv;
-      sm.E[j] = (uint8_t)e;
-      sm.flag[j] = 0;
+      for (int i = 0; i < 4; ++i) y[i] = __fmul_rn(y[i], scale);
+      float n2 = __fmul_rn(y[0], y[0]);
+      n2 = __fmaf_rn(y[1], y[1], n2);
+      n2 = __fmaf_rn(y[2], y[2], n2);
+      n2 = __fmaf_rn(y[3], y[3], n2);
+      n2 = warp_sum(n2);
+      const float iv = n2 > 0.f ? rsqrtf(n2) : 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) macc[i] = __dadd_rn(macc[i], (double)__fmul_rn(y[i], iv));
+      if (lane == 0) {
+        sm.inv[j] = iv;
+        sm.E[j] = (uint8_t)e;
+        sm.flag[j] = 0;
+      }
     }
   }
   if (__syncthreads_or(bad) && tid == 0) latch(P.status, BKV_ERR_NONFINITE);
@@ -218,14 +235,21 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
   __syncthreads();
 
   // ---- phase B: mean cosines a_j = u_j . mbar
-  for (int j = warp; j < N; j += kWarps) {
-    float u[4];
-    unit4(j, u);
-    float a = __fmul_rn(u[0], sm.mvec[4 * lane]);
+  for (int j0 = warp; j0 < N; j0 += kWarps * kBatch) {
+    uint2 wb[kBatch];
+    fetch(j0, wb);
 #pragma unroll
-    for (int i = 1; i < 4; ++i) a = __fmaf_rn(u[i], sm.mvec[4 * lane + i], a);
-    a = warp_sum(a);
-    if (lane == 0) sm.S[j] = a;
+    for (int b = 0; b < kBatch; ++b) {
+      const int j = j0 + b * kWarps;
+      if (j >= N) break;
+      float u[4];
+      unit4(j, wb[b], u);
+      float a = __fmul_rn(u[0], sm.mvec[4 * lane]);
+#pragma unroll
+      for (int i = 1; i < 4; ++i) a = __fmaf_rn(u[i], sm.mvec[4 * lane + i], a);
+      a = warp_sum(a);
+      if (lane == 0) sm.S[j] = a;
+    }
   }
   __syncthreads();
 
@@ -328,20 +352,27 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
     }
     if (warp == 0) {
       float u[4];
-      unit4(r, u);
+      unit4(r, __ldg(reinterpret_cast<const uint2*>(row(r)) + lane), u);
 #pragma unroll
       for (int i = 0; i < 4; ++i) sm.up[4 * lane + i] = u[i];
     }
     __syncthreads();
     if (k + 1 < m) {
-      for (int j = warp; j < N; j += kWarps) {
-        float u[4];
-        unit4(j, u);
-        float c = __fmul_rn(u[0], sm.up[4 * lane]);
+      for (int j0 = warp; j0 < N; j0 += kWarps * kBatch) {
+        uint2 wb[kBatch];
+        fetch(j0, wb);
 #pragma unroll
-        for (int i = 1; i < 4; ++i) c = __fmaf_rn(u[i], sm.up[4 * lane + i], c);
-        c = warp_sum(c);
-        if (lane == 0) sm.S[j] = k == 0 ? c : fmaxf(sm.S[j], c);
+        for (int b = 0; b < kBatch; ++b) {
+          const int j = j0 + b * kWarps;
+          if (j >= N) break;
+          float u[4];
+          unit4(j, wb[b], u);
+          float c = __fmul_rn(u[0], sm.up[4 * lane]);
+#pragma unroll
+          for (int i = 1; i < 4; ++i) c = __fmaf_rn(u[i], sm.up[4 * lane + i], c);
+          c = warp_sum(c);
+          if (lane == 0) sm.S[j] = k == 0 ? c : fmaxf(sm.S[j], c);
+        }
       }
       __syncthreads();
     }
