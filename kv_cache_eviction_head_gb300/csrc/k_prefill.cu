@@ -3,7 +3,9 @@
 // sampled from the input queries). Of the P prompt queries, the last
 // nr = min(n_rq, P) go to the recent ring at their own positions and the
 // beacons are FPS (Algorithm 1) of the N = P - nr older ones, keeping
-// m = min(fps_keep, N). One CTA of 128 threads per head.
+// m = min(fps_keep, N). One CTA per head: 256 threads with the candidates'
+// rows resident in shared memory when they fit (N up to ~790), else 128
+// threads reading them from global memory on every pass.
 //
 // FPS over N candidates (up to thousands) in O(N d m) instead of the O(N^2 d)
 // of a Gram matrix:
@@ -13,6 +15,15 @@
 //   * the mean cosine a_i = (1/N) sum_j cos(x_i, x_j) = u_i . mbar with
 //     mbar = (1/N) sum_j u_j, accumulated in float64 and rounded to float32;
 //   * every pick round refreshes S_j = max(S_j, u_j . u_r) in one pass.
+// With the rows resident, each row is stored once more as y_j = x_j 2^s_j in
+// bf16 (exact: a power-of-two scaling, apart from components more than ~126
+// binades below the row's largest, which round in the bf16 subnormal range,
+// < 2^-126 each against a largest component >= 1), and the passes give each
+// thread whole candidates: c_j = (y_j . v) / ||y_j|| with the float32 dot in
+// four partial sums of 32 products (gamma_35 = 2.1e-6 relative to
+// ||y_j|| ||v||), so |c32 - cos| <= 4e-6 for v a computed unit vector and
+// |a32 - a64| <= 4e-6 plus the reference's summation error, within the same
+// filter bounds.
 // Error bounds (relative to unit vectors, so absolute on cosines): u_j carries
 // <= 5.7e-7 per component (norm: 4 FMAs and a 5-level tree, gamma_9; rsqrtf
 // 2 ulp; one multiply), a float32 dot adds gamma_9; so |c32 - cos| <= 2e-6 and
@@ -31,9 +42,9 @@ namespace bkv {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kWarps = kThreads / 32;
-constexpr int kBatch = 8;  // candidates per warp whose row loads are in flight together
+constexpr int kMaxWarps = 8;
+constexpr int kRowStride = kD * 2 + 16;  // bytes per resident row: 16-byte reads of 8 consecutive rows hit distinct banks
+constexpr int kBatch = 8;                // candidates per warp whose row loads are in flight together
 constexpr float kCosErr = 2e-5f;
 constexpr float kMeanErr = 2.5e-5f;
 constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -57,27 +68,31 @@ struct PfSmem {
   float* S;         // [N] mean cosine, then the running max cosine to the picks
   uint8_t* E;       // [N] largest biased exponent of the row (sets s_j)
   uint8_t* flag;    // [N] bit 0 picked, bit 1 close candidate
-  double* mpart;    // [kWarps][kD] per-warp sums of unit vectors
+  double* mpart;    // [warps][kD] per-warp sums of unit vectors
   float* mvec;      // [kD] mean unit vector, float32
   float* up;        // [kD] unit vector of the latest pick
-  double* xv;       // [kWarps][32] exact values, one chunk per warp
-  double* bestv;    // [kWarps]
-  int* besti;       // [kWarps]
-  uint32_t* red;    // [kWarps] reduction scratch
+  double* xv;       // [warps][32] exact values, one chunk per warp
+  double* bestv;    // [warps]
+  int* besti;       // [warps]
+  uint32_t* red;    // [warps] reduction scratch
+  unsigned char* rows;  // resident: [N][kRowStride] scaled rows, bf16
   int* picks;       // [32]
   int* ctl;         // [4] broadcast words
 };
 
-__host__ __device__ inline size_t pf_smem_bytes(int N) {
-  size_t b = (size_t)N * 10;
+__host__ __device__ inline size_t pf_smem_bytes(int N, bool resident) {
+  size_t b = resident ? (size_t)N * kRowStride : 0;
+  b += (size_t)N * 10;
   b = (b + 15) / 16 * 16;
-  return b + (size_t)kWarps * kD * 8 + kD * 4 * 2 + kWarps * 32 * 8 + kWarps * 8 + kWarps * 4 +
-         kWarps * 4 + 32 * 4 + 16 + 64;
+  return b + (size_t)kMaxWarps * kD * 8 + kD * 4 * 2 + kMaxWarps * 32 * 8 + kMaxWarps * 8 + kMaxWarps * 4 +
+         kMaxWarps * 4 + 32 * 4 + 16 + 64;
 }
 
-__device__ inline PfSmem pf_carve(unsigned char* base, int N) {
+__device__ inline PfSmem pf_carve(unsigned char* base, int N, bool resident) {
   PfSmem s;
   size_t off = 0;
+  s.rows = base;
+  if (resident) off += (size_t)N * kRowStride;
   s.inv = reinterpret_cast<float*>(base + off);
   off += (size_t)N * 4;
   s.S = reinterpret_cast<float*>(base + off);
@@ -88,19 +103,19 @@ __device__ inline PfSmem pf_carve(unsigned char* base, int N) {
   off += N;
   off = (off + 15) / 16 * 16;
   s.mpart = reinterpret_cast<double*>(base + off);
-  off += (size_t)kWarps * kD * 8;
+  off += (size_t)kMaxWarps * kD * 8;
   s.xv = reinterpret_cast<double*>(base + off);
-  off += (size_t)kWarps * 32 * 8;
+  off += (size_t)kMaxWarps * 32 * 8;
   s.bestv = reinterpret_cast<double*>(base + off);
-  off += kWarps * 8;
+  off += kMaxWarps * 8;
   s.mvec = reinterpret_cast<float*>(base + off);
   off += kD * 4;
   s.up = reinterpret_cast<float*>(base + off);
   off += kD * 4;
   s.besti = reinterpret_cast<int*>(base + off);
-  off += kWarps * 4;
+  off += kMaxWarps * 4;
   s.red = reinterpret_cast<uint32_t*>(base + off);
-  off += kWarps * 4;
+  off += kMaxWarps * 4;
   s.picks = reinterpret_cast<int*>(base + off);
   off += 32 * 4;
   s.ctl = reinterpret_cast<int*>(base + off);
@@ -134,12 +149,36 @@ __device__ double cos64_rows(const uint4* ri, int ei, bool wi, double gii, const
   return __ddiv_rn(g, __dsqrt_rn(__dmul_rn(gii, gjj)));
 }
 
+// The resident variant's per-candidate dot: y_j (scaled bf16 row in shared
+// memory) with a float32 vector v, four partial sums of 32 products.
+__device__ __forceinline__ float resident_dot(const unsigned char* yrow, const float* v) {
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < kD / 8; ++c) {
+    const uint4 w = *reinterpret_cast<const uint4*>(yrow + c * 16);
+    const float4 v0 = *reinterpret_cast<const float4*>(v + 8 * c);
+    const float4 v1 = *reinterpret_cast<const float4*>(v + 8 * c + 4);
+    a0 = __ffma2_rn(make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u)),
+                    make_float2(v0.x, v0.y), a0);
+    a1 = __ffma2_rn(make_float2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u)),
+                    make_float2(v0.z, v0.w), a1);
+    a0 = __ffma2_rn(make_float2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u)),
+                    make_float2(v1.x, v1.y), a0);
+    a1 = __ffma2_rn(make_float2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u)),
+                    make_float2(v1.z, v1.w), a1);
+  }
+  return __fadd_rn(__fadd_rn(a0.x, a0.y), __fadd_rn(a1.x, a1.y));
+}
+
+template <int kThreads, bool kResident>
 __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
+  constexpr int kWarps = kThreads / 32;
+  static_assert(kWarps <= kMaxWarps, "shared-memory plan");
   extern __shared__ __align__(16) unsigned char pf_smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t head = blockIdx.x;
   const int N = P.N, m = P.m;
-  PfSmem sm = pf_carve(pf_smem, N);
+  PfSmem sm = pf_carve(pf_smem, N, kResident);
   auto row = [&](int j) -> const uint4* { return P.q + ((int64_t)j * P.heads_total + head) * 16; };
   uint4* bq = P.bq + head * P.fps_cap * 16;
   uint4* rq = P.rq + head * P.n_rq * 16;
@@ -165,7 +204,10 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int j = j0 + b * kWarps;
-      w[b] = j < N ? __ldg(reinterpret_cast<const uint2*>(row(j)) + lane) : make_uint2(0u, 0u);
+      if (kResident)
+        w[b] = j < N ? *reinterpret_cast<const uint2*>(sm.rows + (size_t)j * kRowStride + lane * 8) : make_uint2(0u, 0u);
+      else
+        w[b] = j < N ? __ldg(reinterpret_cast<const uint2*>(row(j)) + lane) : make_uint2(0u, 0u);
     }
   };
   // lane's four components of a row as float32 (the bf16 values), and their largest biased exponent
@@ -189,7 +231,26 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
     for (int i = 0; i < 4; ++i) u[i] = __fmul_rn(__fmul_rn(y[i], scale), iv);
   };
 
-  // ---- phase A: scaling, norms, flags, sum of unit vectors
+  if (kResident) {
+    // ---- phase 0: the candidates' rows into shared memory, 8 loads in flight per thread
+    for (int i0 = tid; i0 < N * 16; i0 += kThreads * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const int i = i0 + b * kThreads;
+        if (i < N * 16) v[b] = __ldg(row(i >> 4) + (i & 15));
+      }
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const int i = i0 + b * kThreads;
+        if (i < N * 16) *reinterpret_cast<uint4*>(sm.rows + (size_t)(i >> 4) * kRowStride + (i & 15) * 16) = v[b];
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- phase A: scaling, norms, flags, sum of unit vectors (resident rows
+  // are rewritten scaled by 2^s_j)
   double macc[4] = {0.0, 0.0, 0.0, 0.0};
   bool bad = false;
   for (int j0 = warp; j0 < N; j0 += kWarps * kBatch) {
@@ -208,6 +269,11 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
       const float scale = __int_as_float(max(254 - (int)e, 1) << 23);
 #pragma unroll
       for (int i = 0; i < 4; ++i) y[i] = __fmul_rn(y[i], scale);
+      if (kResident) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]), hi = __floats2bfloat162_rn(y[2], y[3]);
+        *reinterpret_cast<uint2*>(sm.rows + (size_t)j * kRowStride + lane * 8) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+      }
       float n2 = __fmul_rn(y[0], y[0]);
       n2 = __fmaf_rn(y[1], y[1], n2);
       n2 = __fmaf_rn(y[2], y[2], n2);
@@ -227,7 +293,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) sm.mpart[warp * kD + 4 * lane + i] = macc[i];
   __syncthreads();
-  {
+  if (tid < kD) {
     double s = 0.0;
     for (int w = 0; w < kWarps; ++w) s = __dadd_rn(s, sm.mpart[w * kD + tid]);
     sm.mvec[tid] = __double2float_rn(__ddiv_rn(s, (double)N));
@@ -235,20 +301,25 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
   __syncthreads();
 
   // ---- phase B: mean cosines a_j = u_j . mbar
-  for (int j0 = warp; j0 < N; j0 += kWarps * kBatch) {
-    uint2 wb[kBatch];
-    fetch(j0, wb);
+  if (kResident) {
+    for (int j = tid; j < N; j += kThreads)
+      sm.S[j] = __fmul_rn(resident_dot(sm.rows + (size_t)j * kRowStride, sm.mvec), sm.inv[j]);
+  } else {
+    for (int j0 = warp; j0 < N; j0 += kWarps * kBatch) {
+      uint2 wb[kBatch];
+      fetch(j0, wb);
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int j = j0 + b * kWarps;
-      if (j >= N) break;
-      float u[4];
-      unit4(j, wb[b], u);
-      float a = __fmul_rn(u[0], sm.mvec[4 * lane]);
+      for (int b = 0; b < kBatch; ++b) {
+        const int j = j0 + b * kWarps;
+        if (j >= N) break;
+        float u[4];
+        unit4(j, wb[b], u);
+        float a = __fmul_rn(u[0], sm.mvec[4 * lane]);
 #pragma unroll
-      for (int i = 1; i < 4; ++i) a = __fmaf_rn(u[i], sm.mvec[4 * lane + i], a);
-      a = warp_sum(a);
-      if (lane == 0) sm.S[j] = a;
+        for (int i = 1; i < 4; ++i) a = __fmaf_rn(u[i], sm.mvec[4 * lane + i], a);
+        a = warp_sum(a);
+        if (lane == 0) sm.S[j] = a;
+      }
     }
   }
   __syncthreads();
@@ -352,12 +423,26 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
     }
     if (warp == 0) {
       float u[4];
-      unit4(r, __ldg(reinterpret_cast<const uint2*>(row(r)) + lane), u);
+      if (kResident) {  // the stored row is already scaled: u = y_r / ||y_r||
+        float y[4];
+        uint32_t e;
+        split4(*reinterpret_cast<const uint2*>(sm.rows + (size_t)r * kRowStride + lane * 8), y, e);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) u[i] = __fmul_rn(y[i], sm.inv[r]);
+      } else {
+        unit4(r, __ldg(reinterpret_cast<const uint2*>(row(r)) + lane), u);
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) sm.up[4 * lane + i] = u[i];
     }
     __syncthreads();
-    if (k + 1 < m) {
+    if (k + 1 < m && kResident) {
+      for (int j = tid; j < N; j += kThreads) {
+        const float c = __fmul_rn(resident_dot(sm.rows + (size_t)j * kRowStride, sm.up), sm.inv[j]);
+        sm.S[j] = k == 0 ? c : fmaxf(sm.S[j], c);
+      }
+      __syncthreads();
+    } else if (k + 1 < m) {
       for (int j0 = warp; j0 < N; j0 += kWarps * kBatch) {
         uint2 wb[kBatch];
         fetch(j0, wb);
@@ -396,15 +481,25 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
 
 }  // namespace
 
-size_t prefill_smem_bytes(int N) { return pf_smem_bytes(N); }
+size_t prefill_smem_bytes(int N) { return pf_smem_bytes(N, false); }
 
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t s) {
   if (p.heads_total <= 0) return cudaSuccess;
-  const size_t smem = pf_smem_bytes(p.N > 0 ? p.N : 1);
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  prefill_kernel<<<(unsigned)p.heads_total, kThreads, smem, s>>>(p);
+  const int n = p.N > 0 ? p.N : 1;
+  const size_t cap = 227 * 1024;
+  const bool resident = pf_smem_bytes(n, true) <= cap;
+  const size_t smem = pf_smem_bytes(n, resident);
+  if (smem > cap) return cudaErrorInvalidValue;
+  cudaError_t e;
+  if (resident) {
+    e = cudaFuncSetAttribute(prefill_kernel<256, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prefill_kernel<256, true><<<(unsigned)p.heads_total, 256, smem, s>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(prefill_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prefill_kernel<128, false><<<(unsigned)p.heads_total, 128, smem, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -314,6 +314,16 @@ def test_prefill_long_prompt_then_large_eviction():
     assert_clean(rep, min_evictions=4)
 
 
+def test_prefill_rows_beyond_shared_memory():
+    """A 900-step prompt: 884 older queries per head do not fit the resident
+    layout (884 x 272 B), so prefill FPS takes the variant that reads the rows
+    from global memory on every pass; queries with wide exponent ranges, zero
+    rows and duplicates included."""
+    w = TINY.with_(cache_slots=900, steps=960)
+    rep = run_lockstep(w, seed=0xBEAD7, prefill=900, query_hook=wide_queries)
+    assert_clean(rep, min_evictions=3)
+
+
 def test_prefill_gqa7_wide_exponents():
     # 96 prompt steps keep the FPS phase of a plain stream: at each eviction a
     # head holds 16 beacons + 16 recents, so 7 heads make 224 observation rows
