@@ -107,6 +107,17 @@ def aggregate(per_rank_evictions: int, elapsed_s_max: float, world: int) -> floa
     return per_rank_evictions * world / elapsed_s_max
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The largest of the ranks' elapsed times: the job ends with its slowest rank."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------------------- byte model
 
 def kernel_bytes(w, R: int, rows_moved_per_launch: float, heads_total: int, n_fps: int) -> dict:
@@ -334,10 +345,7 @@ def run_ours(args, w):
     bkv.bkv_profile(h, False)
     bkv.bkv_sync(h)
     st1 = bkv.bkv_get_stats(h)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     evictions_per_step = w.evictions_per_round
     value = aggregate(evictions_per_step * args.steps, elapsed_ms / 1e3, world)
 
@@ -391,10 +399,7 @@ def run_ours(args, w):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, w, bkv, h, K, V, kept, kptr, vptr, qpool[n_periods:], state, dev, cs)
-        if world > 1:
-            tt = torch.tensor([e2e["elapsed_ms"]], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e["elapsed_ms"] = float(tt.item())
+        e2e["elapsed_ms"] = max_over_ranks(e2e["elapsed_ms"], world, dev)
         e2e = {"value": aggregate(evictions_per_step * e2e["steps"], e2e["elapsed_ms"] / 1e3, world),
                "unit": "evictions/s", "h2d_bytes_per_step": e2e["h2d"],
                "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"]}
