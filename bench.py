@@ -375,9 +375,9 @@ def run_ours(args, w):
     # ---- future-query coverage of the observation sets (diagnostic, untimed step)
     coverage = None
     if args.coverage > 0:
-        g = torch.Generator(device=dev).manual_seed(99)
-        qf = torch.randn(args.coverage, w.layers, w.batch, w.heads, w.d, generator=g,
-                         device=dev).to(torch.bfloat16)
+        # the stream's next queries (the synthetic recipe), as the observation
+        # sets would meet them
+        qf = torch.stack([stream.queries() for _ in range(args.coverage)])
         cov = torch.empty(w.layers, w.batch, w.heads, args.coverage, dtype=torch.float64, device=dev)
         for _ in range(2):
             bkv.bkv_coverage(h, qf, cov)
@@ -410,8 +410,11 @@ def run_ours(args, w):
     prefill = None
     if args.prefill > 0:
         P = min(args.prefill, w.max_cache)
-        gq = torch.Generator(device=dev).manual_seed(7)
-        qp = torch.randn(P, w.layers, w.batch, w.heads, w.d, generator=gq, device=dev).to(torch.bfloat16)
+        # a prompt from a fresh stream of the same synthetic recipe
+        pstream = SyntheticStream(w, seed=0xBEAC0 + 7, device=dev)
+        qp = torch.empty(P, w.layers, w.batch, w.heads, w.d, dtype=torch.bfloat16, device=dev)
+        for i in range(P):
+            qp[i] = pstream.queries()
         ms = []
         for rep in range(4):
             ws2 = torch.empty(bkv.bkv_workspace_bytes(cfg), dtype=torch.uint8, device=dev)

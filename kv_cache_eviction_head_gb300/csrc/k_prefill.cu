@@ -3,8 +3,8 @@
 // sampled from the input queries). Of the P prompt queries, the last
 // nr = min(n_rq, P) go to the recent ring at their own positions and the
 // beacons are FPS (Algorithm 1) of the N = P - nr older ones, keeping
-// m = min(fps_keep, N). One CTA per head: 256 threads with the candidates'
-// rows resident in shared memory when they fit (N up to ~790), else 128
+// m = min(fps_keep, N). One CTA per head: 512 threads with the candidates'
+// rows resident in shared memory when they fit (N up to ~750), else 128
 // threads reading them from global memory on every pass.
 //
 // FPS over N candidates (up to thousands) in O(N d m) instead of the O(N^2 d)
@@ -13,7 +13,10 @@
 //     (power-of-two scaling as in the FPS kernel, then rsqrtf); each warp
 //     takes one candidate at a time, lane l holding dimensions 4l..4l+3;
 //   * the mean cosine a_i = (1/N) sum_j cos(x_i, x_j) = u_i . mbar with
-//     mbar = (1/N) sum_j u_j, accumulated in float64 and rounded to float32;
+//     mbar = (1/N) sum_j u_j, each lane's share summed in float32 with a
+//     compensation term (Kahan), the warps' partials merged in float64, then
+//     rounded to float32 (the compensated sum errs by <= 2^-23 sum |u_jk|,
+//     i.e. < 3e-8 per component after the division by N, < 3.4e-7 on a_i);
 //   * every pick round refreshes S_j = max(S_j, u_j . u_r) in one pass.
 // With the rows resident, each row is stored once more as y_j = x_j 2^s_j in
 // bf16 (exact: a power-of-two scaling, apart from components more than ~126
@@ -22,12 +25,12 @@
 // thread whole candidates: c_j = (y_j . v) / ||y_j|| with the float32 dot in
 // four partial sums of 32 products (gamma_35 = 2.1e-6 relative to
 // ||y_j|| ||v||), so |c32 - cos| <= 4e-6 for v a computed unit vector and
-// |a32 - a64| <= 4e-6 plus the reference's summation error, within the same
+// |a32 - a64| <= 4.5e-6 plus the reference's summation error, within the same
 // filter bounds.
 // Error bounds (relative to unit vectors, so absolute on cosines): u_j carries
 // <= 5.7e-7 per component (norm: 4 FMAs and a 5-level tree, gamma_9; rsqrtf
 // 2 ulp; one multiply), a float32 dot adds gamma_9; so |c32 - cos| <= 2e-6 and
-// |a32 - a64| <= 2e-6 plus the float64 reference's own summation error
+// |a32 - a64| <= 2.5e-6 plus the float64 reference's own summation error
 // (<= N 2^-53). The filters use kCosErr = 2e-5 and kMeanErr = 2.5e-5: a pick
 // is final when the float32 minimum beats every other candidate by twice the
 // bound; otherwise the exact float64 values of the close candidates (exact dot
@@ -42,7 +45,7 @@ namespace bkv {
 
 namespace {
 
-constexpr int kMaxWarps = 8;
+constexpr int kMaxWarps = 16;
 constexpr int kRowStride = kD * 2 + 16;  // bytes per resident row: 16-byte reads of 8 consecutive rows hit distinct banks
 constexpr int kBatch = 8;                // candidates per warp whose row loads are in flight together
 constexpr float kCosErr = 2e-5f;
@@ -67,7 +70,7 @@ struct PfSmem {
   float* inv;       // [N] 1 / ||x_j 2^s_j||
   float* S;         // [N] mean cosine, then the running max cosine to the picks
   uint8_t* E;       // [N] largest biased exponent of the row (sets s_j)
-  uint8_t* flag;    // [N] bit 0 picked, bit 1 close candidate
+  uint8_t* flag;    // [N] bit 0: picked
   double* mpart;    // [warps][kD] per-warp sums of unit vectors
   float* mvec;      // [kD] mean unit vector, float32
   float* up;        // [kD] unit vector of the latest pick
@@ -77,7 +80,8 @@ struct PfSmem {
   uint32_t* red;    // [warps] reduction scratch
   unsigned char* rows;  // resident: [N][kRowStride] scaled rows, bf16
   int* picks;       // [32]
-  int* ctl;         // [4] broadcast words
+  int* cntw;        // [warps] close candidates per warp
+  int* lastw;       // [warps] the largest of them
 };
 
 __host__ __device__ inline size_t pf_smem_bytes(int N, bool resident) {
@@ -85,7 +89,7 @@ __host__ __device__ inline size_t pf_smem_bytes(int N, bool resident) {
   b += (size_t)N * 10;
   b = (b + 15) / 16 * 16;
   return b + (size_t)kMaxWarps * kD * 8 + kD * 4 * 2 + kMaxWarps * 32 * 8 + kMaxWarps * 8 + kMaxWarps * 4 +
-         kMaxWarps * 4 + 32 * 4 + 16 + 64;
+         kMaxWarps * 4 + 32 * 4 + 2 * kMaxWarps * 4 + 64;
 }
 
 __device__ inline PfSmem pf_carve(unsigned char* base, int N, bool resident) {
@@ -118,7 +122,9 @@ __device__ inline PfSmem pf_carve(unsigned char* base, int N, bool resident) {
   off += kMaxWarps * 4;
   s.picks = reinterpret_cast<int*>(base + off);
   off += 32 * 4;
-  s.ctl = reinterpret_cast<int*>(base + off);
+  s.cntw = reinterpret_cast<int*>(base + off);
+  off += kMaxWarps * 4;
+  s.lastw = reinterpret_cast<int*>(base + off);
   return s;
 }
 
@@ -251,7 +257,8 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
 
   // ---- phase A: scaling, norms, flags, sum of unit vectors (resident rows
   // are rewritten scaled by 2^s_j)
-  double macc[4] = {0.0, 0.0, 0.0, 0.0};
+  // compensated float32 sums (Kahan): float64 adds are scarce on this part
+  float msum[4] = {0.f, 0.f, 0.f, 0.f}, mcomp[4] = {0.f, 0.f, 0.f, 0.f};
   bool bad = false;
   for (int j0 = warp; j0 < N; j0 += kWarps * kBatch) {
     uint2 wb[kBatch];
@@ -281,7 +288,12 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
       n2 = warp_sum(n2);
       const float iv = n2 > 0.f ? rsqrtf(n2) : 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) macc[i] = __dadd_rn(macc[i], (double)__fmul_rn(y[i], iv));
+      for (int i = 0; i < 4; ++i) {
+        const float x = __fsub_rn(__fmul_rn(y[i], iv), mcomp[i]);
+        const float t = __fadd_rn(msum[i], x);
+        mcomp[i] = __fsub_rn(__fsub_rn(t, msum[i]), x);
+        msum[i] = t;
+      }
       if (lane == 0) {
         sm.inv[j] = iv;
         sm.E[j] = (uint8_t)e;
@@ -291,7 +303,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
   }
   if (__syncthreads_or(bad) && tid == 0) latch(P.status, BKV_ERR_NONFINITE);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) sm.mpart[warp * kD + 4 * lane + i] = macc[i];
+  for (int i = 0; i < 4; ++i) sm.mpart[warp * kD + 4 * lane + i] = (double)msum[i] - (double)mcomp[i];
   __syncthreads();
   if (tid < kD) {
     double s = 0.0;
@@ -336,26 +348,35 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
     uint32_t all = sm.red[0];
     for (int w = 1; w < kWarps; ++w) all = min(all, sm.red[w]);
     const float lim = unkey(all) + 2.0f * err;
+    // close candidates: each warp publishes its count and its largest one,
+    // so one barrier gives every thread the total (and, if it is 1, the pick)
     int cnt = 0, last = -1;
     for (int j = tid; j < N; j += kThreads)
       if (!(sm.flag[j] & 1) && sm.S[j] <= lim) {
         ++cnt;
         last = j;
-        sm.flag[j] |= 2;
       }
-    const int holders = __syncthreads_count(cnt > 0);  // threads holding a close candidate
-    const int several = __syncthreads_count(cnt > 1);  // threads holding more than one
+    const int wcnt = (int)__reduce_add_sync(kFull, (uint32_t)cnt);
+    const int wlast = __reduce_max_sync(kFull, last);
+    if (lane == 0) {
+      sm.cntw[warp] = wcnt;
+      sm.lastw[warp] = wlast;
+    }
+    __syncthreads();
+    int total = 0, only = -1;
+    for (int w = 0; w < kWarps; ++w) {
+      total += sm.cntw[w];
+      if (sm.cntw[w] == 1) only = sm.lastw[w];
+    }
     int pick;
-    if (holders == 1 && several == 0) {
-      if (cnt) sm.ctl[0] = last;
-      __syncthreads();
-      pick = sm.ctl[0];
+    if (total == 1) {
+      pick = only;
     } else {
       // each warp evaluates the close candidates of its residue class exactly
       double bv = 0.0;
       int bi = -1;
       for (int i = warp; i < N; i += kWarps) {
-        if (!(sm.flag[i] & 2)) continue;  // uniform across the warp
+        if ((sm.flag[i] & 1) || !(sm.S[i] <= lim)) continue;  // uniform across the warp
         const uint4* ri = row(i);
         int ei;
         bool wi;
@@ -409,8 +430,6 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(PrefillParams P) {
       }
       if (pick < 0) pick = 0;  // only with NaN inputs, which are latched
     }
-    for (int j = tid; j < N; j += kThreads) sm.flag[j] &= 1;
-    __syncthreads();
     return pick;
   };
 
@@ -492,9 +511,9 @@ cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t s) {
   if (smem > cap) return cudaErrorInvalidValue;
   cudaError_t e;
   if (resident) {
-    e = cudaFuncSetAttribute(prefill_kernel<256, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(prefill_kernel<512, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    prefill_kernel<256, true><<<(unsigned)p.heads_total, 256, smem, s>>>(p);
+    prefill_kernel<512, true><<<(unsigned)p.heads_total, 512, smem, s>>>(p);
   } else {
     e = cudaFuncSetAttribute(prefill_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
