@@ -53,6 +53,8 @@
 // order like the values: each lane keeps a sorted list of its smallest
 // (score bits, ~slot) keys, the warp extracts the D smallest from the list
 // heads, and a ballot scan writes the kept (and dropped) slots in order.
+#include <atomic>
+
 #include "score_common.cuh"
 
 namespace bkv {
@@ -976,16 +978,17 @@ size_t score_smem_bytes(int R, int L, int nr, int budget, int compact) {
 
 bool encode_kmaps(ScoreParams& p, const void* const* K, int layers, int batch, int kv_heads,
                   int max_cache) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (!encode) {
+  // the driver's encoder, looked up once per process (thread-safe static initialisation)
+  static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
     cudaDriverEntryPointQueryResult qres;
     void* fn = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qres) !=
             cudaSuccess ||
-        qres != cudaDriverEntryPointSuccess || !fn)
-      return false;
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
+        qres != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }();
+  if (!encode) return false;
   const cuuint64_t rows = (cuuint64_t)batch * kv_heads * max_cache;
   const cuuint64_t dims[2] = {(cuuint64_t)kD, rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
@@ -1003,20 +1006,21 @@ bool encode_kmaps(ScoreParams& p, const void* const* K, int layers, int batch, i
 
 cudaError_t launch_score_select(const ScoreParams& p, cudaStream_t s) {
   const size_t smem = score_smem_bytes(p.group * (p.nb + p.nr), p.L, p.nr, p.budget, p.compact);
-  static size_t configured = 0;
-  if (smem > configured) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(score_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  // the largest plan once per device (one bit each); every launch then fits
+  static std::atomic<unsigned long long> configured{0};
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (!(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(score_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
-    configured = smem;
+    configured.fetch_or(bit);
   }
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
-  }
-  const int grid = p.units < sms ? p.units : sms;
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = p.units < sms ? p.units : sms;  // one persistent CTA per SM
   score_select_kernel<<<grid, kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
