@@ -276,9 +276,10 @@ def run_ours(args, w):
     from synth import SyntheticStream
 
     stream = SyntheticStream(w, seed=0xBEAC0 + 2, device=dev)
-    K = [torch.empty(w.batch, w.kv_heads, w.max_cache, w.d, dtype=torch.bfloat16, device=dev)
-         for _ in range(w.layers)]
-    V = [torch.empty_like(K[0]) for _ in range(w.layers)]
+    # one allocation per tensor for all layers; the library takes per-layer views
+    K_all = torch.empty(w.layers, w.batch, w.kv_heads, w.max_cache, w.d, dtype=torch.bfloat16, device=dev)
+    V_all = torch.empty_like(K_all)
+    K, V = list(K_all.unbind(0)), list(V_all.unbind(0))
     for l in range(w.layers):
         stream.fill_cache(K[l], V[l], l, w.max_cache)
     kept = torch.empty(w.layers, w.batch, w.kv_heads, w.budget, dtype=torch.int32, device=dev)
@@ -398,7 +399,7 @@ def run_ours(args, w):
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, bkv, h, K, V, kept, kptr, vptr, qpool[n_periods:], state, dev, cs)
+        e2e = run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, qpool[n_periods:], state, dev, cs)
         e2e["elapsed_ms"] = max_over_ranks(e2e["elapsed_ms"], world, dev)
         e2e = {"value": aggregate(evictions_per_step * e2e["steps"], e2e["elapsed_ms"] / 1e3, world),
                "unit": "evictions/s", "h2d_bytes_per_step": e2e["h2d"],
@@ -488,7 +489,7 @@ def run_ours(args, w):
     return 0
 
 
-def run_e2e(args, w, bkv, h, K, V, kept, kptr, vptr, qpool, state, dev, cs):
+def run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, qpool, state, dev, cs):
     """Same step through the C ABI, with each step's inputs coming from pinned
     host memory (the period's queries and the new K/V rows) and the keep sets
     going back to the host, all inside the timed region. The copies run on a
@@ -499,9 +500,8 @@ def run_e2e(args, w, bkv, h, K, V, kept, kptr, vptr, qpool, state, dev, cs):
     import torch
     q_host = qpool.cpu().pin_memory()  # one period of queries per step, host side
     tail = torch.empty(w.layers, 2, w.batch, w.kv_heads, w.period, w.d, dtype=torch.bfloat16)
-    for l in range(w.layers):
-        tail[l, 0] = K[l][:, :, w.budget:w.max_cache].cpu()
-        tail[l, 1] = V[l][:, :, w.budget:w.max_cache].cpu()
+    tail[:, 0] = K_all[:, :, :, w.budget:w.max_cache].cpu()
+    tail[:, 1] = V_all[:, :, :, w.budget:w.max_cache].cpu()
     tail = tail.pin_memory()
     n_periods = q_host.shape[0]
     xs = torch.cuda.Stream(dev)
@@ -533,9 +533,8 @@ def run_e2e(args, w, bkv, h, K, V, kept, kptr, vptr, qpool, state, dev, cs):
             kept_host[b].copy_(kept_dev[b], non_blocking=True)
             ev["read"][b].record(xs)
         cs.wait_event(ev["staged"][b])
-        for l in range(w.layers):
-            K[l][:, :, w.budget:w.max_cache].copy_(tstage[b][l, 0], non_blocking=True)
-            V[l][:, :, w.budget:w.max_cache].copy_(tstage[b][l, 1], non_blocking=True)
+        K_all[:, :, :, w.budget:w.max_cache].copy_(tstage[b][:, 0], non_blocking=True)
+        V_all[:, :, :, w.budget:w.max_cache].copy_(tstage[b][:, 1], non_blocking=True)
         for i in range(w.period):
             bkv.bkv_append_queries(h, qstage[b][i], t + 1 + i)
         ev["used"][b].record(cs)
