@@ -266,6 +266,15 @@ bkv_status bkv_score_select_noalloc(const bkv_config* cfg, const void* bq, const
                                     int32_t cache_len, int64_t step, int32_t* kept,
                                     void* cuda_stream);
 
+/* Self-test of the bounded device-side waits every kernel uses (the timeout
+ * latch and the abort of the other waiting warps): enqueues on the handle's
+ * stream a kernel whose four warps wait up to wait_cycles SM clock cycles
+ * (1 .. 2e9; the kernels' own limit is 2e9, about a second) on a barrier that
+ * nothing completes. The next bkv_sync then returns BKV_ERR_TIMEOUT and
+ * clears it; the stream, the handle and its state stay usable. Nothing else
+ * is touched. BKV_ERR_INVALID_ARG for a limit out of range. */
+bkv_status bkv_selftest_wait(bkv_handle h, int64_t wait_cycles);
+
 /* Counters and bookkeeping; synchronizes to read the device counter. */
 bkv_status bkv_get_stats(bkv_handle h, bkv_stats* out);
 

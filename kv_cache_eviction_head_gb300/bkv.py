@@ -34,7 +34,7 @@ BKV_FLAG_ORDER_FREE = 2
 BKV_FLAG_MEAN_POOL = 4
 
 EXPORTED = ["bkv_workspace_bytes", "bkv_create", "bkv_set_stream", "bkv_append_queries",
-            "bkv_evict", "bkv_prefill", "bkv_coverage", "bkv_sync", "bkv_get_fps_trace", "bkv_get_scores", "bkv_get_head_state",
+            "bkv_evict", "bkv_prefill", "bkv_coverage", "bkv_selftest_wait", "bkv_sync", "bkv_get_fps_trace", "bkv_get_scores", "bkv_get_head_state",
             "bkv_profile", "bkv_profile_read", "bkv_score_select_noalloc", "bkv_get_stats",
             "bkv_destroy", "bkv_status_str"]
 KERNELS = ["append", "rope", "score_select", "fps", "coverage", "prefill"]
@@ -68,6 +68,7 @@ _lib.bkv_evict.argtypes = [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, 
 _lib.bkv_coverage.argtypes = [_vp, _vp, _i32, _vp]
 _lib.bkv_prefill.argtypes = [_vp, _vp, _i32, _i64, _vp]
 _lib.bkv_sync.argtypes = [_vp]
+_lib.bkv_selftest_wait.argtypes = [_vp, _i64]
 _lib.bkv_get_fps_trace.argtypes = [_vp, _vp, _sz]
 _lib.bkv_get_scores.argtypes = [_vp, _vp, _sz]
 _lib.bkv_get_head_state.argtypes = [_vp, _i32, _i32, _i32, _vp, _sz]
@@ -176,6 +177,11 @@ def bkv_coverage(h: Handle, q_future, out) -> None:
 
 def bkv_sync(h: Handle) -> None:
     _check(_lib.bkv_sync(_vp(h.ptr)), "bkv_sync")
+
+
+def bkv_selftest_wait(h: Handle, wait_cycles: int) -> None:
+    """Enqueues the bounded-wait self-test; the next bkv_sync raises BKV_ERR_TIMEOUT."""
+    _check(_lib.bkv_selftest_wait(_vp(h.ptr), _i64(wait_cycles)), "bkv_selftest_wait")
 
 
 def bkv_get_fps_trace(h: Handle) -> np.ndarray:

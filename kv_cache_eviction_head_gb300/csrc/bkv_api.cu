@@ -362,6 +362,13 @@ bkv_status bkv_coverage(bkv_handle h, const void* q_future, int32_t n_future, do
   return BKV_OK;
 }
 
+bkv_status bkv_selftest_wait(bkv_handle h, int64_t wait_cycles) {
+  if (!h || wait_cycles < 1 || wait_cycles > 2000000000LL) return BKV_ERR_INVALID_ARG;
+  if (bkv::launch_wait_selftest(h->status(), (long long)wait_cycles, h->stream) != cudaSuccess)
+    return BKV_ERR_CUDA;
+  return BKV_OK;
+}
+
 bkv_status bkv_sync(bkv_handle h) {
   if (!h) return BKV_ERR_INVALID_ARG;
   uint32_t code = 0;

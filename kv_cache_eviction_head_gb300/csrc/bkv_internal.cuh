@@ -111,6 +111,8 @@ struct ScoreParams {
   int pool_mean;  // 1: Score[j] = mean over the observation rows of W[., j] (Table 2)
 };
 cudaError_t launch_score_select(const ScoreParams& p, cudaStream_t s);
+// Four warps wait `limit` cycles on a barrier nothing completes (see bkv_selftest_wait).
+cudaError_t launch_wait_selftest(uint32_t* status, long long limit, cudaStream_t s);
 // Dynamic shared memory the score kernel needs (huge when the shape does not fit).
 size_t score_smem_bytes(int R, int L, int nr, int budget, int compact);
 // Fills p.kmap for K[0..layers) (host; no device allocation). False on failure.

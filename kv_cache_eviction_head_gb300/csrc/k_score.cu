@@ -976,6 +976,31 @@ size_t score_smem_bytes(int R, int L, int nr, int budget, int compact) {
   return s.stages >= 2 ? s.total : (size_t)1 << 30;  // no plan fits: not supported
 }
 
+namespace {
+
+// Self-test of the bounded waits: four warps wait on an mbarrier that nothing
+// arrives on; the first to run out latches BKV_ERR_TIMEOUT and raises the
+// abort flag, which the others see at their next poll. Every thread exits.
+__global__ void __launch_bounds__(128) wait_selftest_kernel(uint32_t* status, long long limit) {
+  __shared__ uint64_t bar;
+  __shared__ Ctl ctl;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    ctl.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const bool ok = mbar_wait(&bar, 0u, &ctl, status, limit);
+  if (ok) latch(status, BKV_ERR_INTERNAL);  // nothing completes the phase
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(uint32_t* status, long long limit, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 128, 0, s>>>(status, limit);
+  return cudaGetLastError();
+}
+
 bool encode_kmaps(ScoreParams& p, const void* const* K, int layers, int batch, int kv_heads,
                   int max_cache) {
   // the driver's encoder, looked up once per process (thread-safe static initialisation)

@@ -49,14 +49,15 @@ struct Ctl {
 };
 
 // Bounded wait for the phase with the given parity. Returns false (after
-// latching the timeout and raising the abort flag) if it never completes, or
-// as soon as another role has aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Ctl* ctl, uint32_t* status) {
+// latching the timeout and raising the abort flag) if it does not complete
+// within `limit` cycles, or as soon as another role has aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Ctl* ctl, uint32_t* status,
+                                          long long limit = kWaitCycles) {
   if (mbar_test(b, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_test(b, parity)) {
     if (ctl->abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       latch(status, BKV_ERR_TIMEOUT);
       ctl->abort = 1;
       return false;

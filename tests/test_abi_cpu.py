@@ -91,7 +91,8 @@ def test_create_rejects_bad_workspace_before_any_cuda_call(bkv):
 def test_null_handle_calls_are_rejected(bkv):
     for name, args in [("bkv_append_queries", (None, None, 0)), ("bkv_sync", (None,)),
                        ("bkv_evict", (None, None, None, 0, 0, None)),
-                       ("bkv_get_fps_trace", (None, None, 0)), ("bkv_set_stream", (None, None))]:
+                       ("bkv_get_fps_trace", (None, None, 0)), ("bkv_set_stream", (None, None)),
+                       ("bkv_selftest_wait", (None, 1000))]:
         assert bkv.raw_status(name, *args) == bkv.BKV_ERR_INVALID_ARG
 
 

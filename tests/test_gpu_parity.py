@@ -432,3 +432,37 @@ def test_nonfinite_query_is_latched_not_trapped():
         bkv.bkv_sync(h)                         # the latch was cleared
     finally:
         bkv.bkv_destroy(h)
+
+
+def test_bounded_wait_runs_out_latches_timeout_and_the_handle_stays_usable():
+    """The bounded device-side waits every kernel uses: four warps wait on a
+    barrier nothing completes (about a millisecond here); the wait that runs
+    out latches BKV_ERR_TIMEOUT, the other warps see the abort flag and leave,
+    and the handle then evicts as usual."""
+    from kv_cache_eviction_head_gb300 import bkv
+    dev = torch.device("cuda")
+    cfg = bkv.make_config(heads=4, kv_heads=1, d=128, budget=64, period=16, prefix=4, recent=16,
+                          fps_cap=32, fps_keep=16, layers=1, batch=1, max_cache=80, rope_theta=1e6)
+    ws = torch.empty(bkv.bkv_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    h = bkv.bkv_create(cfg, ws, torch.cuda.current_stream())
+    try:
+        with pytest.raises(bkv.BkvError) as e:
+            bkv.bkv_selftest_wait(h, 0)
+        assert e.value.code == bkv.BKV_ERR_INVALID_ARG
+        bkv.bkv_selftest_wait(h, 2_000_000)
+        with pytest.raises(bkv.BkvError) as e:
+            bkv.bkv_sync(h)
+        assert e.value.code == bkv.BKV_ERR_TIMEOUT
+        bkv.bkv_sync(h)  # the latch was cleared
+        g = torch.Generator(device=dev).manual_seed(3)
+        K = [torch.randn(1, 1, 80, 128, generator=g, device=dev).to(torch.bfloat16)]
+        V = [torch.randn(1, 1, 80, 128, generator=g, device=dev).to(torch.bfloat16)]
+        kept = torch.empty(1, 1, 1, 64, dtype=torch.int32, device=dev)
+        for t in range(80):
+            bkv.bkv_append_queries(h, torch.randn(1, 1, 4, 128, generator=g, device=dev).to(torch.bfloat16), t)
+        bkv.bkv_evict(h, K, V, 80, 79, kept)
+        bkv.bkv_sync(h)
+        k = kept[0, 0, 0].tolist()
+        assert len(k) == 64 and k == sorted(set(k)) and k[:4] == [0, 1, 2, 3] and k[-16:] == list(range(64, 80))
+    finally:
+        bkv.bkv_destroy(h)
