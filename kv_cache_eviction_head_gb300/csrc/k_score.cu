@@ -332,9 +332,9 @@ __host__ __device__ inline Layout make_layout(int Rtot, int L, int nr, int budge
   off += (size_t)s.chunks * s.qrows * 8;
   s.drops = off;
   off += 2 * (size_t)s.D * 4 + 16;
-  s.bars = (off + 7) & ~(size_t)7;
+  s.bars = (off + 15) & ~(size_t)15;
   off = s.bars + 64 * 8;
-  s.misc = off;
+  s.misc = off;  // 16-byte aligned: the copier keeps int4 chunk descriptors here
   off += kMiscBytes;
   s.total = off + 1024;
   return s;

@@ -61,6 +61,33 @@ def test_tiny_variants(name, over):
     assert_clean(rep)
 
 
+@pytest.mark.parametrize("order_free", [False, True])
+def test_odd_drop_count(order_free):
+    """17 drops per unit (period 17): odd drop counts, which shift the shared
+    memory that follows the drop lists by 8 bytes."""
+    w = TINY.with_(period=17, steps=260)
+    rep = run_lockstep(w, seed=0xBEAB6, order_free=order_free)
+    assert_clean(rep, min_evictions=5)
+
+
+def test_period_one_drops_one_slot_per_step():
+    """An eviction after every append: L = budget + 1, one slot dropped, FPS over
+    the beacons and a single recent query each time."""
+    w = TINY.with_(period=1, steps=200)
+    rep = run_lockstep(w, seed=0xBEAB7)
+    assert_clean(rep, min_evictions=60)
+
+
+@pytest.mark.parametrize("budget,period", [(8176, 16), (7680, 512)])
+def test_longest_cache_8192_slots(budget, period):
+    """The longest cache the kernels take (L = 8192: 64 tiles, the selector's
+    8192-bit drop mask; the shared-memory plan falls back to fewer compaction
+    chunks), with 16 drops per unit (per-lane lists) and with 512 (radix)."""
+    w = TINY.with_(budget=budget, period=period, steps=8192 + 2 * period)
+    rep = run_lockstep(w, seed=0xBEAB8 + period)
+    assert_clean(rep, min_evictions=2)
+
+
 def test_many_tiles():
     w = TINY.with_(budget=1000, steps=1100, heads=8, kv_heads=2)
     rep = run_lockstep(w, seed=7)
