@@ -301,10 +301,10 @@ def run_ours(args, w):
         bkv.bkv_append_queries(h, stream.queries(), t)
     # every period gets the stream's next queries (a repeated period would hand
     # FPS exact duplicates, which no decode stream produces)
-    n_periods = args.warmup + args.steps          # device-resident runs use [0, n_periods)
-    qpool = torch.empty(2 * n_periods, w.period, w.layers, w.batch, w.heads, w.d, dtype=torch.bfloat16,
+    n_periods = args.warmup + args.steps
+    qpool = torch.empty(n_periods, w.period, w.layers, w.batch, w.heads, w.d, dtype=torch.bfloat16,
                         device=dev)
-    for p in range(2 * n_periods):             # the e2e run uses the second half
+    for p in range(n_periods):
         for i in range(w.period):
             qpool[p, i] = stream.queries()
     bkv.bkv_sync(h)
@@ -399,7 +399,8 @@ def run_ours(args, w):
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, qpool[n_periods:], state, dev, cs)
+        del qpool
+        e2e = run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, stream, state, dev, cs)
         e2e["elapsed_ms"] = max_over_ranks(e2e["elapsed_ms"], world, dev)
         e2e = {"value": aggregate(evictions_per_step * e2e["steps"], e2e["elapsed_ms"] / 1e3, world),
                "unit": "evictions/s", "h2d_bytes_per_step": e2e["h2d"],
@@ -489,23 +490,40 @@ def run_ours(args, w):
     return 0
 
 
-def run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, qpool, state, dev, cs):
+def run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, stream, state, dev, cs,
+            host_cap_bytes=48 << 30):
     """Same step through the C ABI, with each step's inputs coming from pinned
     host memory (the period's queries and the new K/V rows) and the keep sets
     going back to the host, all inside the timed region. The copies run on a
     second stream, double-buffered, so that step k + 1's inputs travel while
     step k's eviction runs: inputs land in device staging buffers, and the new
     K/V rows move into the cache (a device copy) once the eviction that reads
-    those slots is done."""
+    those slots is done.
+
+    Every step gets a period of fresh queries from the stream (a repeated
+    period would hand FPS exact duplicates), generated before the timed region
+    straight into pinned host memory. The pool is capped at host_cap_bytes; a
+    workload whose periods do not fit runs fewer e2e steps (one warm-up and at
+    least one timed), and the returned step count says so."""
     import torch
-    q_host = qpool.cpu().pin_memory()  # one period of queries per step, host side
-    tail = torch.empty(w.layers, 2, w.batch, w.kv_heads, w.period, w.d, dtype=torch.bfloat16)
-    tail[:, 0] = K_all[:, :, :, w.budget:w.max_cache].cpu()
-    tail[:, 1] = V_all[:, :, :, w.budget:w.max_cache].cpu()
-    tail = tail.pin_memory()
-    n_periods = q_host.shape[0]
+    per_period = w.period * w.layers * w.batch * w.heads * w.d * 2
+    warm, steps = max(1, args.warmup), args.steps
+    fit = max(2, host_cap_bytes // per_period)
+    if warm + steps > fit:
+        warm, steps = 1, fit - 1
+    total = warm + steps
+    q_host = torch.empty(total, w.period, w.layers, w.batch, w.heads, w.d, dtype=torch.bfloat16,
+                         pin_memory=True)
+    for p in range(total):
+        for i in range(w.period):
+            q_host[p, i].copy_(stream.queries())
+    # the new K/V rows of a period, host side (per layer: small device temporaries)
+    tail = torch.empty(w.layers, 2, w.batch, w.kv_heads, w.period, w.d, dtype=torch.bfloat16, pin_memory=True)
+    for l in range(w.layers):
+        tail[l, 0].copy_(K_all[l, :, :, w.budget:w.max_cache])
+        tail[l, 1].copy_(V_all[l, :, :, w.budget:w.max_cache])
     xs = torch.cuda.Stream(dev)
-    qstage = [torch.empty_like(qpool[0]) for _ in range(2)]
+    qstage = [torch.empty(q_host.shape[1:], dtype=q_host.dtype, device=dev) for _ in range(2)]
     tstage = [torch.empty(tail.shape, dtype=tail.dtype, device=dev) for _ in range(2)]
     kept_dev = [kept, torch.empty_like(kept)]
     kept_host = [torch.empty(kept.shape, dtype=kept.dtype).pin_memory() for _ in range(2)]
@@ -517,7 +535,7 @@ def run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, qpool, state, dev, 
         with torch.cuda.stream(xs):
             if k >= 2:
                 xs.wait_event(ev["used"][b])  # step k - 2 is done with this buffer
-            qstage[b].copy_(q_host[k % n_periods], non_blocking=True)
+            qstage[b].copy_(q_host[k], non_blocking=True)
             tstage[b].copy_(tail, non_blocking=True)
             ev["staged"][b].record(xs)
 
@@ -540,17 +558,16 @@ def run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, qpool, state, dev, 
         ev["used"][b].record(cs)
         state["t"] = t + w.period
 
-    total = max(1, args.warmup) + args.steps
     stage(0)
     stage(1)
-    for k in range(max(1, args.warmup)):
+    for k in range(warm):
         step(k)
         if k + 2 < total:
             stage(k + 2)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(cs)
-    for k in range(max(1, args.warmup), total):
+    for k in range(warm, total):
         step(k)
         if k + 2 < total:
             stage(k + 2)
@@ -558,7 +575,7 @@ def run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, qpool, state, dev, 
     e1.record(cs)
     torch.cuda.synchronize(dev)
     bkv.bkv_sync(h)
-    return {"elapsed_ms": e0.elapsed_time(e1), "steps": args.steps,
+    return {"elapsed_ms": e0.elapsed_time(e1), "steps": steps,
             "h2d": qstage[0].numel() * 2 + tail.numel() * 2, "d2h": kept_host[0].numel() * 4}
 
 

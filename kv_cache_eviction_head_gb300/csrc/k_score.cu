@@ -342,6 +342,9 @@ __host__ __device__ inline Layout make_layout(int Rtot, int L, int nr, int budge
 
 }  // namespace
 
+// kChunked: more than 256 observation rows, scored in row chunks; the
+// single-chunk instance compiles without the chunk bookkeeping.
+template <bool kChunked>
 __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_constant__ ScoreParams P) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
@@ -350,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   const int per_head = P.nb + P.nr;
   const Layout lay = make_layout(P.group * per_head, P.L, P.nr, P.budget, P.compact);
   const int R = lay.R, L = P.L, T = lay.ntiles, S = lay.stages;
+  const int NC = kChunked ? lay.chunks : 1;  // row chunks
 
   unsigned char* q_hi = smem + lay.q_hi;
   unsigned char* q_lo = smem + lay.q_lo;
@@ -407,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
   for (int i = tid; i < (int)(2 * (lay.q_lo - lay.q_hi) / 16); i += kThreads)
     reinterpret_cast<uint4*>(q_hi)[i] = make_uint4(0, 0, 0, 0);
   // per-launch tables, chunk by chunk: the key bound and the source of each row
-  for (int c = 0; c < lay.chunks; ++c)
+  for (int c = 0; c < NC; ++c)
     fill_row_tables(lim + c * lay.rows64, rowinfo + c * lay.qrows, c * R, R, lay.Rtot, lay.rows64, lay.qrows,
                     P.nb, P.nr, L, P.fps_cap, P.n_rq, P.ring_first, tid, kThreads);
   const uint32_t ncols = 2 * (uint32_t)lay.bufcols;
@@ -454,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
         int layer, seq, kvh;
         unit_geom(blockIdx.x + it * gridDim.x, P.batch, P.kv_heads, layer, seq, kvh);
         const int row0 = (seq * P.kv_heads + kvh) * P.max_cache;
-        for (int s2 = 0; s2 < 2 * T * lay.chunks; ++s2) {
+        for (int s2 = 0; s2 < 2 * T * NC; ++s2) {
           const int s = s2 % (2 * T);  // each row chunk runs both passes
           if (g >= S && !mbar_wait(&kempty[st], kph ^ 1u, ctl, P.status)) {
             ok = false;
@@ -493,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       const uint32_t id1 = idesc_bf16(128, 128), id2 = idesc_bf16(128, lay.Rp16);
       int ci = 0;  // row chunks started
       for (int it = 0; it < mine && ok; ++it) {
-        for (int c = 0; c < lay.chunks && ok; ++c, ++ci) {
+        for (int c = 0; c < NC && ok; ++c, ++ci) {
           ok = mbar_wait(qready, (uint32_t)(ci & 1), ctl, P.status);
           for (int s = 0; s < 2 * T && ok; ++s, ++g) {
             const int b = (int)(g & 1);
@@ -722,13 +726,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       // ---------------------------------------------------------- L2 warmer
       // Pulls the next row chunk's source rows into L2 while the current one
       // is scored, so the row build at the chunk boundary reads from L2.
-      const int nchunks = mine * lay.chunks;
+      const int nchunks = mine * NC;
       for (int ci = 0; ci + 1 < nchunks; ++ci) {
         const bool ok = __all_sync(kFull, mbar_wait(qready, (uint32_t)(ci & 1), ctl, P.status));
         if (!ok) break;
-        const int64_t h1 = head_base((ci + 1) / lay.chunks);
+        const int64_t h1 = head_base((ci + 1) / NC);
         for (int r = lane; r < R; r += 32) {
-          const char* src = reinterpret_cast<const char*>(row_src(h1, (ci + 1) % lay.chunks, r));
+          const char* src = reinterpret_cast<const char*>(row_src(h1, (ci + 1) % NC, r));
           if (!src) continue;
           asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
           asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128));
@@ -768,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const float neg_inf = __int_as_float(0xff800000u);
     const float inv_rows = 1.0f / (float)lay.Rtot;  // mean pooling
-    const int C = lay.chunks;
+    const int C = NC;
     long long g = 0;
     bool ok = true;
     int ci = 0;                // row chunks done
@@ -1030,23 +1034,29 @@ bool encode_kmaps(ScoreParams& p, const void* const* K, int layers, int batch, i
 }
 
 cudaError_t launch_score_select(const ScoreParams& p, cudaStream_t s) {
-  const size_t smem = score_smem_bytes(p.group * (p.nb + p.nr), p.L, p.nr, p.budget, p.compact);
+  const int rows = p.group * (p.nb + p.nr);
+  const size_t smem = score_smem_bytes(rows, p.L, p.nr, p.budget, p.compact);
+  const bool chunked = rows > 256;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  // the largest plan once per device (one bit each); every launch then fits
-  static std::atomic<unsigned long long> configured{0};
+  // the largest plan once per device and instance (one bit each); every launch then fits
+  static std::atomic<unsigned long long> configured[2] = {{0}, {0}};
   const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
-  if (!(configured.load() & bit)) {
-    e = cudaFuncSetAttribute(score_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (!(configured[chunked].load() & bit)) {
+    e = chunked ? cudaFuncSetAttribute(score_select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)
+                : cudaFuncSetAttribute(score_select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
-    configured.fetch_or(bit);
+    configured[chunked].fetch_or(bit);
   }
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int grid = p.units < sms ? p.units : sms;  // one persistent CTA per SM
-  score_select_kernel<<<grid, kThreads, smem, s>>>(p);
+  if (chunked)
+    score_select_kernel<true><<<grid, kThreads, smem, s>>>(p);
+  else
+    score_select_kernel<false><<<grid, kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
