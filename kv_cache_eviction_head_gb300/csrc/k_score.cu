@@ -252,13 +252,13 @@ __device__ bool select_keep(const float* sc, int L, int prefix, int recent, int 
 }
 
 // Miscellaneous shared memory: control word [0, 64), dropped-slot bitmask
-// [64, 1088) (L <= 8192), copier chunk descriptors [1536, 1664), order-free
-// pairs [1664, 1920), radix histogram of the selector [2048, 3072).
+// [64, 1088) (L <= 8192), copier chunk descriptors [1536, 1664), radix
+// histogram of the selector [2048, 3072).
 constexpr int kMiscBytes = 3072;
 constexpr int kChunkRows = 32;                   // rows per compaction chunk
 constexpr int kChunkBytes = kChunkRows * kD * 2;  // 8 KB
-constexpr int kPfRows = 512;                      // L2 prefetch lead of the copier (few chunk buffers only)
-constexpr int kPfPieceRows = 64;                  // rows per L2 prefetch
+constexpr int kPfChunks = 16;                     // L2 prefetch lead of the copier in windows (few chunk buffers only)
+constexpr int kRoundChunks = 2;                   // slot-order windows per copier round (<= half the chunk buffers)
 
 struct Layout {
   int Rtot, chunks;                    // observation rows of a unit, row chunks of <= 256
@@ -557,168 +557,325 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       // ---------------------------------------------------------- in-place compaction
       // BeaconKV reading notes §2.3 eq. 8: K_hat = K[:, I_final], V_hat = V[:, I_final].
       // With the dropped slots d_0 < ... < d_{D-1}, the rows of run r,
-      // (d_r, d_{r+1}), move down by r + 1 slots; rows below d_0 stay. Each run
-      // goes through shared memory in chunks of kChunkRows rows with bulk
-      // copies, in increasing address order. A chunk's store overlaps only
-      // sources that were loaded before it (its own and earlier chunks'), and
-      // every later load reads above every earlier store's destination, so
-      // loads may run ahead of stores. One lane issues everything; its buffer
-      // and phase counters wrap without division, since a 64-bit modulo per
-      // chunk costs more than the copy issue itself.
-      if (lane == 0) {
+      // (d_r, d_{r+1}), move down by r + 1 slots; rows below d_0 stay. Every
+      // row's destination lies below its source, so when chunks are loaded in
+      // increasing address order and each chunk is stored only after every
+      // load up to its own has landed, a store overlaps only sources already
+      // loaded, and every later load reads above every earlier store's
+      // destination: loads may run ahead of stores.
+      //
+      // Long runs (L >= 64 D): one lane walks the runs in chunks of up to
+      // kChunkRows rows, one bulk load and one bulk store per chunk, with up
+      // to CB - 1 chunks loaded ahead; a chunk buffer is reloaded once the
+      // store issued before the last one is done reading it. Its buffer and
+      // phase counters wrap without division, since a 64-bit modulo per chunk
+      // costs more than the copy issue itself.
+      //
+      // Short runs: the moved range (d_0, L) goes through shared memory in
+      // windows of kChunkRows consecutive source rows at fixed offsets from
+      // d_0 + 1 (one bulk load each, whatever runs they span); each run's part
+      // of a window leaves with its own bulk store, the dropped rows skipped.
+      // The whole warp issues: a round is up to RW windows, one per lane, and
+      // the chunk buffers form S sets of RW, one set per round, with the loads
+      // of the next S - 1 rounds in flight. Lane i always uses buffer i of a
+      // set, so its own bulk groups tell when its buffer is free again. A
+      // round's stores start once every load of the round has landed.
+      //
+      // Order-free compaction: the k-th dropped slot below the budget (a hole)
+      // receives the k-th kept slot at or above the budget. Sources and
+      // destinations are disjoint, so rounds need no ordering. A round is one
+      // window of 32 tail slots [budget + 32m, budget + 32m + 32): each lane
+      // whose slot is kept copies its K and V rows into a set of two buffers
+      // (K rows, V rows) and from there into its hole.
+      {
         const int CB = lay.cbufs, D = lay.D;
-        int4* cdesc = reinterpret_cast<int4*>(smem + lay.misc + 1536);  // [cbufs] tensor, source row, rows, shift
-        int lb = 0, sb = 0;  // next buffer to load into / to store from (loads and stores cycle alike)
-        uint32_t sph = 0;    // parity of buffer sb's next completion
-        uint32_t ofph[2] = {0u, 0u};  // order-free: parity of buffers 0 and 1's next completion
+        const bool ofree = P.compact == 2;
+        const bool runs = !ofree && (long long)L >= 64LL * D;  // long runs: one lane, chunks along the runs
+        const int RW = ofree ? 32 : (CB / 2 < kRoundChunks ? CB / 2 : kRoundChunks);  // chunks per round
+        const int S = ofree ? CB / 2 : CB / RW;                                       // buffer sets
+        uint32_t par = 0u;  // bit x: parity of the next completion of this lane's buffer in set x (order-free: the set's)
+        int4* cdesc = reinterpret_cast<int4*>(smem + lay.misc + 1536);  // long runs: [cbufs] tensor, source row, rows, shift
+        int lb = 0, sb = 0;  // long runs: next buffer to load into / to store from
+        uint32_t sph = 0u;   // long runs: parity of buffer sb's next completion
         bool ok = true;
         const uint64_t stream = policy_evict_first();
+        // number of dropped slots below x (dl ascending)
+        auto drops_below = [&](const int* dl, int x) -> int {
+          int lo = 0, hi = D;
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (dl[mid] < x)
+              lo = mid + 1;
+            else
+              hi = mid;
+          }
+          return lo;
+        };
         for (int it = 0; it < mine && ok; ++it) {
           const int b = it & 1;
-          ok = mbar_wait(&dready[b], (uint32_t)((it >> 1) & 1), ctl, P.status);
+          ok = __all_sync(kFull, mbar_wait(&dready[b], (uint32_t)((it >> 1) & 1), ctl, P.status));
           if (!ok) break;
           const int* dl = dlist + b * D;
           int layer, seq, kvh;
           unit_geom(blockIdx.x + it * gridDim.x, P.batch, P.kv_heads, layer, seq, kvh);
           const size_t rowbase = (size_t)(seq * P.kv_heads + kvh) * P.max_cache;
-          char* tb[2] = {reinterpret_cast<char*>(P.Kc[layer] + rowbase * kD),
-                         reinterpret_cast<char*>(P.Vc[layer] + rowbase * kD)};
+          char* const tk = reinterpret_cast<char*>(P.Kc[layer] + rowbase * kD);
+          char* const tv = reinterpret_cast<char*>(P.Vc[layer] + rowbase * kD);
+          bulk_wait_read<0>();  // the previous unit's stores are done reading this lane's buffers
+          __syncwarp();
+          uint32_t inflight = 0u;  // bit x: this lane (order-free: the warp) has a load in flight in set x
           unsigned long long moved = 0;  // rows moved per tensor
-          if (P.compact == 2) {
-            // Order-free compaction: the k-th dropped slot below the budget (a
-            // hole) receives the k-th kept slot at or above the budget. Sources
-            // and destinations are disjoint, so chunks need no ordering; K rows
-            // go through chunk buffer 0 and V rows through buffer 1.
-            int h = 0;
-            while (h < D && dl[h] < P.budget) ++h;
-            int2* pairs = reinterpret_cast<int2*>(smem + lay.misc + 1664);  // [kChunkRows] (source, hole)
-            int r = h, x = P.budget;  // next dropped slot at or above the budget; next tail slot
-            for (int k0 = 0; k0 < h && ok; k0 += kChunkRows) {
-              const int n = h - k0 < kChunkRows ? h - k0 : kChunkRows;
-              bulk_wait_read<0>();  // earlier stores are done reading both buffers
-              for (int i = 0; i < n; ++i) {
-                while (r < D && dl[r] == x) {
-                  ++r;
-                  ++x;
-                }
-                pairs[i] = make_int2(x++, dl[k0 + i]);
-              }
-              for (int t2 = 0; t2 < 2; ++t2) {
-                mbar_expect_tx(&cfull[t2], (uint32_t)n * (kD * 2));
-                for (int i = 0; i < n; ++i)
-                  bulk_load(smem_u32(cst + (size_t)t2 * kChunkBytes + (size_t)i * (kD * 2)),
-                            tb[t2] + (size_t)pairs[i].x * (kD * 2), kD * 2, &cfull[t2], stream);
-              }
-              const bool w0 = mbar_wait(&cfull[0], ofph[0], ctl, P.status);
-              const bool w1 = w0 && mbar_wait(&cfull[1], ofph[1], ctl, P.status);
-              if (!w1) {  // loads already issued must land before the CTA exits
-                for (int t2 = 0; t2 < 2; ++t2) {
-                  const long long t0 = clock64();
-                  while (!mbar_test(&cfull[t2], ofph[t2]) && clock64() - t0 < kWaitCycles) {
+          if (runs) {
+            if (lane == 0) {
+              const int first = D > 0 ? dl[0] + 1 : L;  // lowest source row that moves
+              // chunk cursor over the runs of K, then of V: tensor ct, run cr, next source row crow
+              int ct = 0, cr = 0, crow = first;
+              auto next = [&](int4& c) -> bool {
+                while (ct < 2 && D > 0) {
+                  const int end = cr + 1 < D ? dl[cr + 1] : L;
+                  if (crow < end) {
+                    const int n = end - crow < kChunkRows ? end - crow : kChunkRows;
+                    c = make_int4(ct, crow, n, cr + 1);  // run cr moves down by cr + 1 slots
+                    crow += n;
+                    return true;
+                  }
+                  if (++cr < D) {
+                    crow = dl[cr] + 1;
+                  } else {
+                    ++ct;
+                    cr = 0;
+                    crow = first;
                   }
                 }
-                ok = false;
-                break;
-              }
-              ofph[0] ^= 1u;
-              ofph[1] ^= 1u;
-              for (int t2 = 0; t2 < 2; ++t2)
-                for (int i = 0; i < n; ++i)
-                  bulk_store(tb[t2] + (size_t)pairs[i].y * (kD * 2),
-                             smem_u32(cst + (size_t)t2 * kChunkBytes + (size_t)i * (kD * 2)), kD * 2, stream);
-              bulk_commit();
-            }
-            moved = (unsigned long long)h;
-          } else {
-            const int first = D > 0 ? dl[0] + 1 : L;  // lowest source row that moves
-            // chunk cursor over the runs of K, then of V: tensor ct, run cr, next source row crow
-            int ct = 0, cr = 0, crow = first;
-            auto next = [&](int4& c) -> bool {
-              while (ct < 2 && D > 0) {
-                const int end = cr + 1 < D ? dl[cr + 1] : L;
-                if (crow < end) {
-                  const int n = end - crow < kChunkRows ? end - crow : kChunkRows;
-                  c = make_int4(ct, crow, n, cr + 1);  // run cr moves down by cr + 1 slots
-                  crow += n;
-                  return true;
+                return false;
+              };
+              // With few chunk buffers the loads alone keep too few bytes in
+              // flight to cover HBM latency; the moved rows [first, L) of K,
+              // then of V, are then prefetched into L2 kPfChunks windows ahead.
+              const bool pf_on = CB <= 4;
+              const int span = L - first;
+              int pf_row = 0;  // rows prefetched so far, K's moved rows then V's
+              auto prefetch_to = [&](int target) {
+                target = target < 2 * span ? target : 2 * span;
+                while (pf_row < target) {
+                  const int pt = pf_row >= span ? 1 : 0;
+                  const int off = pf_row - (pt ? span : 0);
+                  int nr = span - off < kChunkRows ? span - off : kChunkRows;
+                  nr = target - pf_row < nr ? target - pf_row : nr;
+                  bulk_prefetch_l2((pt ? tv : tk) + (size_t)(first + off) * (kD * 2), (uint32_t)nr * (kD * 2));
+                  pf_row += nr;
                 }
-                if (++cr < D) {
-                  crow = dl[cr] + 1;
-                } else {
-                  ++ct;
-                  cr = 0;
-                  crow = first;
-                }
-              }
-              return false;
-            };
-            // With few chunk buffers the loads alone keep too few bytes in
-            // flight to cover HBM latency; the moved rows [first, L) of K, then
-            // of V, are then prefetched into L2 kPfRows rows ahead of them.
-            const bool pf_on = CB <= 4;
-            const int span = L - first;
-            int pf_row = 0;  // rows prefetched so far, K's moved rows then V's
-            auto prefetch_to = [&](int target) {
-              target = target < 2 * span ? target : 2 * span;
-              while (pf_row < target) {
-                const int pt = pf_row >= span ? 1 : 0;
-                const int off = pf_row - (pt ? span : 0);
-                int nr = span - off < kPfPieceRows ? span - off : kPfPieceRows;
-                nr = target - pf_row < nr ? target - pf_row : nr;
-                bulk_prefetch_l2(tb[pt] + (size_t)(first + off) * (kD * 2), (uint32_t)nr * (kD * 2));
-                pf_row += nr;
-              }
-            };
-            if (pf_on) prefetch_to(kPfRows);
-            auto load = [&](const int4& c) {
-              cdesc[lb] = c;
-              const uint32_t bytes = (uint32_t)c.z * (kD * 2);
-              mbar_expect_tx(&cfull[lb], bytes);
-              bulk_load(smem_u32(cst + (size_t)lb * kChunkBytes), tb[c.x] + (size_t)c.y * (kD * 2), bytes, &cfull[lb],
-                        stream);
-              lb = lb + 1 == CB ? 0 : lb + 1;
-              if (pf_on) prefetch_to((c.x ? span : 0) + c.y + c.z - first + kPfRows);
-            };
-            bulk_wait_read<0>();  // the previous unit's stores are done reading every chunk buffer
-            int inflight = 0;
-            int4 c;
-            while (inflight < CB - 1 && next(c)) {
-              load(c);
-              ++inflight;
-            }
-            while (inflight > 0) {
-              ok = mbar_wait(&cfull[sb], sph, ctl, P.status);
-              if (!ok) break;
-              const int4 d = cdesc[sb];
-              bulk_store(tb[d.x] + (size_t)(d.y - d.w) * (kD * 2), smem_u32(cst + (size_t)sb * kChunkBytes),
-                         (uint32_t)d.z * (kD * 2), stream);
-              bulk_commit();
-              if (++sb == CB) {
-                sb = 0;
-                sph ^= 1u;
-              }
-              --inflight;
-              if (next(c)) {
-                bulk_wait_read<1>();  // the buffer reused now belonged to the store before the last one
+              };
+              if (pf_on) prefetch_to(kPfChunks * kChunkRows);
+              auto load = [&](const int4 c) {
+                cdesc[lb] = c;
+                const uint32_t bytes = (uint32_t)c.z * (kD * 2);
+                mbar_expect_tx(&cfull[lb], bytes);
+                bulk_load(smem_u32(cst + (size_t)lb * kChunkBytes), (c.x ? tv : tk) + (size_t)c.y * (kD * 2), bytes,
+                          &cfull[lb], stream);
+                lb = lb + 1 == CB ? 0 : lb + 1;
+                if (pf_on) prefetch_to((c.x ? span : 0) + c.y + c.z - first + kPfChunks * kChunkRows);
+              };
+              int pend = 0;
+              int4 c;
+              while (pend < CB - 1 && next(c)) {
                 load(c);
-                ++inflight;
+                ++pend;
               }
-            }
-            if (!ok) {  // after an abort, loads already issued must land before the CTA exits
-              for (; inflight > 0; --inflight) {
-                const long long t0 = clock64();
-                while (!mbar_test(&cfull[sb], sph) && clock64() - t0 < kWaitCycles) {
-                }
+              while (pend > 0) {
+                ok = mbar_wait(&cfull[sb], sph, ctl, P.status);
+                if (!ok) break;
+                const int4 d = cdesc[sb];
+                bulk_store((d.x ? tv : tk) + (size_t)(d.y - d.w) * (kD * 2), smem_u32(cst + (size_t)sb * kChunkBytes),
+                           (uint32_t)d.z * (kD * 2), stream);
+                bulk_commit();
                 if (++sb == CB) {
                   sb = 0;
                   sph ^= 1u;
                 }
+                --pend;
+                if (next(c)) {
+                  bulk_wait_read<1>();  // the buffer reused now belonged to the store before the last one
+                  load(c);
+                  ++pend;
+                }
+              }
+              if (!ok) {  // after an abort, loads already issued must land before the CTA exits
+                for (; pend > 0; --pend) {
+                  const long long t0 = clock64();
+                  while (!mbar_test(&cfull[sb], sph) && clock64() - t0 < kWaitCycles) {
+                  }
+                  if (++sb == CB) {
+                    sb = 0;
+                    sph ^= 1u;
+                  }
+                }
+              }
+              moved = D > 0 ? (unsigned long long)(L - D - dl[0]) : 0ull;
+            }
+            ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+          } else if (!ofree) {
+            const int first = D > 0 ? dl[0] + 1 : L;  // lowest source row that moves
+            const int W = (L - first + kChunkRows - 1) / kChunkRows;  // windows per tensor
+            const int nch = D > 0 ? 2 * W : 0;                        // K windows, then V windows
+            const int nrounds = (nch + RW - 1) / RW;
+            // With few chunk buffers the loads alone keep too few bytes in
+            // flight to cover HBM latency; the windows kPfChunks ahead are then
+            // prefetched into L2.
+            const bool pf_on = CB <= 4;
+            auto window = [&](int j, char*& src, int& s, int& n) {
+              const bool v = j >= W;
+              src = v ? tv : tk;
+              s = first + (v ? j - W : j) * kChunkRows;
+              n = L - s < kChunkRows ? L - s : kChunkRows;
+            };
+            if (pf_on && lane < kPfChunks && lane < nch) {
+              char* src;
+              int s0, n;
+              window(lane, src, s0, n);
+              bulk_prefetch_l2(src + (size_t)s0 * (kD * 2), (uint32_t)n * (kD * 2));
+            }
+            auto issue = [&](int g) {
+              const int j = g * RW + lane, set = g % S;
+              if (lane < RW && j < nch) {
+                char* src;
+                int s0, n;
+                window(j, src, s0, n);
+                const int bi = set * RW + lane;
+                mbar_expect_tx(&cfull[bi], (uint32_t)n * (kD * 2));
+                bulk_load(smem_u32(cst + (size_t)bi * kChunkBytes), src + (size_t)s0 * (kD * 2),
+                          (uint32_t)n * (kD * 2), &cfull[bi], stream);
+                inflight |= 1u << set;
+                if (pf_on && j + kPfChunks < nch) {
+                  window(j + kPfChunks, src, s0, n);
+                  bulk_prefetch_l2(src + (size_t)s0 * (kD * 2), (uint32_t)n * (kD * 2));
+                }
+              }
+            };
+            for (int g = 0; g < S - 1 && g < nrounds; ++g) issue(g);
+            for (int g = 0; g < nrounds; ++g) {
+              const int j = g * RW + lane, set = g % S;
+              const bool act = lane < RW && j < nch;
+              if (S == 1) issue(g);  // a single set: its previous stores were drained below
+              bool mok = true;
+              if (act) {
+                mok = mbar_wait(&cfull[set * RW + lane], (par >> set) & 1u, ctl, P.status);
+                if (mok) {
+                  par ^= 1u << set;
+                  inflight &= ~(1u << set);
+                }
+              }
+              ok = __all_sync(kFull, mok);
+              if (!ok) break;
+              if (act) {
+                // the kept rows of window j, one bulk store per run
+                char* dst;
+                int s0, n;
+                window(j, dst, s0, n);
+                const uint32_t buf = smem_u32(cst + (size_t)(set * RW + lane) * kChunkBytes);
+                const int end = s0 + n;
+                int r = drops_below(dl, s0), seg = s0;
+                for (;;) {
+                  const int stop = r < D && dl[r] < end ? dl[r] : end;
+                  if (stop > seg)
+                    bulk_store(dst + (size_t)(seg - r) * (kD * 2), buf + (uint32_t)(seg - s0) * (kD * 2),
+                               (uint32_t)(stop - seg) * (kD * 2), stream);
+                  if (stop == end) break;
+                  seg = stop + 1;
+                  ++r;
+                }
+              }
+              bulk_commit();
+              if (S == 1) {
+                bulk_wait_read<0>();
+              } else if (g + S - 1 < nrounds) {
+                bulk_wait_read<1>();  // round g - 1's stores are done reading the set reloaded now
+                issue(g + S - 1);
               }
             }
             moved = D > 0 ? (unsigned long long)(L - D - dl[0]) : 0ull;
+          } else {
+            const int h = drops_below(dl, P.budget);  // holes
+            const int nrounds = (L - P.budget + 31) / 32;
+            // lane's tail slot in round m, whether it is kept, and its rank
+            // among the kept tail slots (= the index of its hole)
+            auto slot = [&](int m, int& x, int& rank) -> bool {
+              x = P.budget + 32 * m + lane;
+              if (x >= L) return false;
+              const int below = drops_below(dl, x);
+              rank = (x - P.budget) - (below - h);
+              return !(below < D && dl[below] == x);
+            };
+            auto issue = [&](int m) {
+              const int set = m % S;
+              int x, rank;
+              const bool kept = slot(m, x, rank);
+              const unsigned bal = __ballot_sync(kFull, kept);
+              if (!bal) return;
+              const int row = __popc(bal & ((1u << lane) - 1u));
+              if (lane == 0) {
+                mbar_expect_tx(&cfull[2 * set], (uint32_t)__popc(bal) * (kD * 2));
+                mbar_expect_tx(&cfull[2 * set + 1], (uint32_t)__popc(bal) * (kD * 2));
+              }
+              __syncwarp();
+              if (kept) {
+                bulk_load(smem_u32(cst + (size_t)(2 * set) * kChunkBytes + (size_t)row * (kD * 2)),
+                          tk + (size_t)x * (kD * 2), kD * 2, &cfull[2 * set], stream);
+                bulk_load(smem_u32(cst + (size_t)(2 * set + 1) * kChunkBytes + (size_t)row * (kD * 2)),
+                          tv + (size_t)x * (kD * 2), kD * 2, &cfull[2 * set + 1], stream);
+              }
+              inflight |= 1u << set;
+            };
+            for (int m = 0; m < S - 1 && m < nrounds; ++m) issue(m);
+            for (int m = 0; m < nrounds; ++m) {
+              const int set = m % S;
+              if (S == 1) issue(m);
+              if (inflight & (1u << set)) {
+                const bool w0 = mbar_wait(&cfull[2 * set], (par >> set) & 1u, ctl, P.status);
+                ok = __all_sync(kFull, w0 && mbar_wait(&cfull[2 * set + 1], (par >> set) & 1u, ctl, P.status));
+                if (!ok) break;
+                par ^= 1u << set;
+                inflight &= ~(1u << set);
+                int x, rank;
+                const bool kept = slot(m, x, rank);
+                const int row = __popc(__ballot_sync(kFull, kept) & ((1u << lane) - 1u));
+                if (kept) {
+                  const int hole = dl[rank];
+                  bulk_store(tk + (size_t)hole * (kD * 2),
+                             smem_u32(cst + (size_t)(2 * set) * kChunkBytes + (size_t)row * (kD * 2)), kD * 2, stream);
+                  bulk_store(tv + (size_t)hole * (kD * 2),
+                             smem_u32(cst + (size_t)(2 * set + 1) * kChunkBytes + (size_t)row * (kD * 2)), kD * 2,
+                             stream);
+                }
+              }
+              bulk_commit();
+              if (S == 1) {
+                bulk_wait_read<0>();
+              } else if (m + S - 1 < nrounds) {
+                bulk_wait_read<1>();  // round m - 1's stores are done reading the set reloaded now
+                issue(m + S - 1);
+              }
+            }
+            moved = (unsigned long long)h;
           }
-          if (ok && moved && P.rows_moved) atomicAdd(P.rows_moved, moved);
-          mbar_arrive(&dfree[b]);
+          if (!ok) {
+            // after an abort, loads already issued must land before the CTA exits
+            for (int set = 0; set < S; ++set) {
+              if (!(inflight & (1u << set))) continue;
+              const int n = ofree ? 2 : 1;
+              for (int q = 0; q < n; ++q) {
+                const int bi = ofree ? 2 * set + q : set * RW + lane;
+                const long long t0 = clock64();
+                while (!mbar_test(&cfull[bi], (par >> set) & 1u) && clock64() - t0 < kWaitCycles) {
+                }
+              }
+            }
+            break;
+          }
+          if (lane == 0) {
+            if (moved && P.rows_moved) atomicAdd(P.rows_moved, moved);
+            mbar_arrive(&dfree[b]);
+          }
         }
         bulk_wait_all();  // every store has landed before the CTA may exit
       }
