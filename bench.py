@@ -490,6 +490,17 @@ def run_ours(args, w):
     return 0
 
 
+def e2e_plan(period_bytes: int, warmup: int, steps: int, host_cap_bytes: int):
+    """(warm-up, timed) steps of the e2e run: one host period of queries per
+    step, at least one warm-up step, and no more periods than host_cap_bytes
+    holds (then one warm-up and the rest timed, at least one)."""
+    warm, timed = max(1, warmup), steps
+    fit = max(2, host_cap_bytes // period_bytes)
+    if warm + timed > fit:
+        warm, timed = 1, fit - 1
+    return warm, timed
+
+
 def run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, stream, state, dev, cs,
             host_cap_bytes=48 << 30):
     """Same step through the C ABI, with each step's inputs coming from pinned
@@ -507,10 +518,7 @@ def run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, stream, state, dev,
     least one timed), and the returned step count says so."""
     import torch
     per_period = w.period * w.layers * w.batch * w.heads * w.d * 2
-    warm, steps = max(1, args.warmup), args.steps
-    fit = max(2, host_cap_bytes // per_period)
-    if warm + steps > fit:
-        warm, steps = 1, fit - 1
+    warm, steps = e2e_plan(per_period, args.warmup, args.steps, host_cap_bytes)
     total = warm + steps
     q_host = torch.empty(total, w.period, w.layers, w.batch, w.heads, w.d, dtype=torch.bfloat16,
                          pin_memory=True)
