@@ -113,7 +113,11 @@ struct bkv_ctx {
   cudaError_t timed(int kernel, cudaStream_t on, F launch) {
     if (!prof) return launch();
     cudaEvent_t a = take_event(), b = take_event();
-    if (!a || !b) return cudaErrorMemoryAllocation;
+    if (!a || !b) {  // keep whichever event was made for later use
+      if (a) pool.push_back(a);
+      if (b) pool.push_back(b);
+      return cudaErrorMemoryAllocation;
+    }
     cudaEventRecord(a, on);
     const cudaError_t e = launch();
     cudaEventRecord(b, on);
