@@ -34,7 +34,8 @@ BKV_FLAG_ORDER_FREE = 2
 BKV_FLAG_MEAN_POOL = 4
 
 EXPORTED = ["bkv_workspace_bytes", "bkv_create", "bkv_set_stream", "bkv_append_queries",
-            "bkv_evict", "bkv_prefill", "bkv_coverage", "bkv_selftest_wait", "bkv_sync", "bkv_get_fps_trace", "bkv_get_scores", "bkv_get_head_state",
+            "bkv_evict", "bkv_prefill", "bkv_coverage", "bkv_selftest_wait", "bkv_sync",
+            "bkv_get_fps_trace", "bkv_get_scores", "bkv_get_head_state",
             "bkv_profile", "bkv_profile_read", "bkv_score_select_noalloc", "bkv_get_stats",
             "bkv_destroy", "bkv_status_str"]
 KERNELS = ["append", "rope", "score_select", "fps", "coverage", "prefill"]
