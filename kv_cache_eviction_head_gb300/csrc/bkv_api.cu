@@ -5,9 +5,20 @@
 #include <new>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "bkv_internal.cuh"
 
 namespace {
+
+// NVTX range over one API call, named after it, for timeline tools (Nsight
+// Systems, ncu --nvtx); without an attached tool a push/pop is a no-op check.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr size_t kAlign = 256;
 constexpr size_t kMaxSmem = 227 * 1024;
@@ -214,6 +225,7 @@ bkv_status bkv_set_stream(bkv_handle h, void* cuda_stream) {
 }
 
 bkv_status bkv_append_queries(bkv_handle h, const void* q_pre, int64_t step) {
+  NvtxRange nvtx("bkv_append_queries");
   if (!h || !q_pre || !aligned(q_pre, 16) || step < 0) return BKV_ERR_INVALID_ARG;
   if (h->last_step >= 0 && step != h->last_step + 1) return BKV_ERR_STATE;
   if (h->cache_len + 1 > h->cfg.max_cache) return BKV_ERR_STATE;
@@ -244,6 +256,7 @@ bkv_status bkv_append_queries(bkv_handle h, const void* q_pre, int64_t step) {
 
 bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache_len, int64_t step,
                      int32_t* kept) {
+  NvtxRange nvtx("bkv_evict");
   if (!h || !K || !V || !kept || !aligned(kept, 4)) return BKV_ERR_INVALID_ARG;
   const bkv_config& c = h->cfg;
   for (int l = 0; l < c.layers; ++l)
@@ -314,6 +327,7 @@ bkv_status bkv_evict(bkv_handle h, void* const* K, void* const* V, int32_t cache
 
 bkv_status bkv_prefill(bkv_handle h, const void* q_prompt, int32_t P, int64_t first_step,
                        int32_t* trace_out) {
+  NvtxRange nvtx("bkv_prefill");
   if (!h || !q_prompt || !aligned(q_prompt, 16) || (trace_out && !aligned(trace_out, 4)) || first_step < 0)
     return BKV_ERR_INVALID_ARG;
   const bkv_config& c = h->cfg;
@@ -347,6 +361,7 @@ bkv_status bkv_prefill(bkv_handle h, const void* q_prompt, int32_t P, int64_t fi
 }
 
 bkv_status bkv_coverage(bkv_handle h, const void* q_future, int32_t n_future, double* out) {
+  NvtxRange nvtx("bkv_coverage");
   if (!h || !q_future || !out || n_future < 1 || !aligned(q_future, 16) || !aligned(out, 8))
     return BKV_ERR_INVALID_ARG;
   bkv::CoverageParams p{};
@@ -367,6 +382,7 @@ bkv_status bkv_coverage(bkv_handle h, const void* q_future, int32_t n_future, do
 }
 
 bkv_status bkv_selftest_wait(bkv_handle h, int64_t wait_cycles) {
+  NvtxRange nvtx("bkv_selftest_wait");
   if (!h || wait_cycles < 1 || wait_cycles > 2000000000LL) return BKV_ERR_INVALID_ARG;
   if (bkv::launch_wait_selftest(h->status(), (long long)wait_cycles, h->stream) != cudaSuccess)
     return BKV_ERR_CUDA;
@@ -374,6 +390,7 @@ bkv_status bkv_selftest_wait(bkv_handle h, int64_t wait_cycles) {
 }
 
 bkv_status bkv_sync(bkv_handle h) {
+  NvtxRange nvtx("bkv_sync");
   if (!h) return BKV_ERR_INVALID_ARG;
   uint32_t code = 0;
   if (cudaMemcpyAsync(&code, h->status(), sizeof(code), cudaMemcpyDeviceToHost, h->stream) !=

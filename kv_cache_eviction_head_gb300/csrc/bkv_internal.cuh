@@ -22,6 +22,21 @@ __device__ __forceinline__ void latch(uint32_t* status, uint32_t code) {
   if (status) atomicCAS(status, 0u, code);
 }
 
+// Bounds-checked build (compiled with -DBKV_CHECKED, libbkv_checked.so): every
+// computed slot, row and offset the kernels index with is tested against its
+// buffer before use; a failed test latches BKV_ERR_INTERNAL and the access is
+// skipped, so a bad index shows up as a status code instead of a fault. In the
+// regular build the test compiles away and the condition is not evaluated.
+#ifdef BKV_CHECKED
+__device__ __forceinline__ bool checked_in_range(bool ok, uint32_t* status) {
+  if (!ok) latch(status, BKV_ERR_INTERNAL);
+  return ok;
+}
+#define BKV_IN_RANGE(cond, status) (::bkv::checked_in_range((cond), (status)))
+#else
+#define BKV_IN_RANGE(cond, status) true
+#endif
+
 // ---------------------------------------------------------------------------
 // append: push one query per query head into its recent ring
 struct AppendParams {

@@ -343,7 +343,8 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta, 6) fps_kernel(FpsParams P) 
       if (lane == 0) sm.picks[k] = r;
     }
     __syncwarp();
-    for (int k = lane; k < m; k += 32) trace[k] = (int8_t)sm.picks[k];
+    for (int k = lane; k < m; k += 32)
+      if (BKV_IN_RANGE(sm.picks[k] >= 0 && sm.picks[k] < n, P.status)) trace[k] = (int8_t)sm.picks[k];
     const unsigned m0 = __ballot_sync(kFull, ch0), m1 = __ballot_sync(kFull, ch1);
     const unsigned lt = (1u << lane) - 1u;
     if (ch0) sm.keep_src[__popc(m0 & lt)] = i0;
@@ -362,7 +363,8 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta, 6) fps_kernel(FpsParams P) 
 #pragma unroll
   for (int q = 0; q < 16; ++q) {
     const int idx = lane + 32 * q;
-    if (idx < kept * 16) buf[q] = row(sm.keep_src[idx >> 4])[idx & 15];
+    if (idx < kept * 16 && BKV_IN_RANGE(sm.keep_src[idx >> 4] >= 0 && sm.keep_src[idx >> 4] < n, P.status))
+      buf[q] = row(sm.keep_src[idx >> 4])[idx & 15];
   }
   __syncwarp();
 #pragma unroll

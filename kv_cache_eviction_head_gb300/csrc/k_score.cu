@@ -65,19 +65,32 @@ namespace {
 // by digit (four 8-bit radix passes over a 256-bin shared histogram of the
 // candidates that match the digits chosen so far); every candidate below it
 // is dropped, and among those equal to it the highest slots fill the rest.
+// Softmax weights share a few exponents, so the lanes of a warp mostly hit
+// the same bin: lanes with equal bins are grouped (match.any) and one of them
+// adds the group's count.
 constexpr int kRadixFrom = 32;
+// Scores are weights in [0, 1]; NaN or +inf comes only from a non-finite
+// input (a +inf logit, for one, turns its row's log-sum-exp into NaN or -inf).
+constexpr float kInf = __builtin_huge_valf();
 __device__ bool radix_drop(const float* sc, int c0, int c1, int D, uint32_t* dropped, int* hist) {
   const int lane = threadIdx.x & 31;
   bool bad = false;
-  for (int j = c0 + lane; j < c1; j += 32) bad |= sc[j] != sc[j];
+  for (int j = c0 + lane; j < c1; j += 32) bad |= !(sc[j] < kInf);  // NaN or +inf
   uint32_t prefix = 0u, mask = 0u;
   int rank = D;  // rank (1-based) of the threshold among candidates matching `prefix`
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = lane; i < 256; i += 32) hist[i] = 0;
     __syncwarp();
-    for (int j = c0 + lane; j < c1; j += 32) {
-      const uint32_t bits = __float_as_uint(sc[j]);
-      if ((bits & mask) == prefix) atomicAdd(&hist[(bits >> shift) & 0xFFu], 1);
+    for (int j0 = c0; j0 < c1; j0 += 32) {
+      const int j = j0 + lane;
+      const uint32_t bits = j < c1 ? __float_as_uint(sc[j]) : 0u;
+      const bool take = j < c1 && (bits & mask) == prefix;
+      const unsigned act = __ballot_sync(kFull, take);
+      if (take) {
+        const uint32_t bin = (bits >> shift) & 0xFFu;
+        const unsigned same = __match_any_sync(act, bin);
+        if ((same & ((1u << lane) - 1u)) == 0u) atomicAdd(&hist[bin], __popc(same));
+      }
     }
     __syncwarp();
     // lane l owns bins [8l, 8l + 8): the digit where the running count reaches rank
@@ -149,7 +162,7 @@ __device__ bool list_drop(const float* sc, int c0, int c1, int D, uint32_t* drop
         k[i] = kNoKey;
         if (j < c1) {
           const float v = sc[j];
-          bad |= v != v;
+          bad |= !(v < kInf);  // NaN or +inf
           const u64 key = ((u64)__float_as_uint(v) << 32) | (uint32_t)~j;
           if (key > after) k[i] = key;
         }
@@ -195,9 +208,12 @@ __device__ bool list_drop(const float* sc, int c0, int c1, int D, uint32_t* drop
 // keys above the last one it gave up. dropped[] is a bitmask over slots;
 // drops[] receives the dropped slots ascending. out[] receives the kept
 // slots ascending, or with order_free the layout of the order-free
-// compaction. Returns true if a score was NaN.
-__device__ bool select_keep(const float* sc, int L, int prefix, int recent, int budget, int32_t* out,
-                            uint32_t* dropped, int* drops, bool order_free, int* hist) {
+// compaction. Returns BKV_OK, BKV_ERR_NONFINITE if a score was NaN or +inf, or
+// BKV_ERR_INTERNAL if the dropped set is not exactly D distinct candidate
+// slots; drops[] then holds the D highest candidates instead, so that
+// everything downstream stays in bounds.
+__device__ uint32_t select_keep(const float* sc, int L, int prefix, int recent, int budget, int32_t* out,
+                                uint32_t* dropped, int* drops, bool order_free, int* hist, uint32_t* status) {
   static_assert(kList == 8, "the list networks are written for 8 keys");
   const int lane = threadIdx.x & 31;
   const int c0 = prefix < L ? prefix : L;
@@ -222,17 +238,39 @@ __device__ bool select_keep(const float* sc, int L, int prefix, int recent, int 
     }
     int pos = dbase + x - c;
     while (bits) {
-      drops[pos++] = w * 32 + __ffs(bits) - 1;
+      if (pos < D) drops[pos] = w * 32 + __ffs(bits) - 1;
+      ++pos;
       bits &= bits - 1;
     }
     dbase += __shfl_sync(kFull, x, 31);
   }
   __syncwarp();
+  // consistency of the keep set: exactly D dropped slots (the kept ones then
+  // number budget), all of them candidates, so the prefix and the recent
+  // window stay kept
+  const bool consistent = dbase == D && (D == 0 || (drops[0] >= c0 && drops[D - 1] < c1));
+  if (!consistent) {
+    __syncwarp();
+    for (int wd = lane; wd < (L + 31) / 32; wd += 32) dropped[wd] = 0u;
+    __syncwarp();
+    for (int i = lane; i < D; i += 32) {
+      drops[i] = c1 - D + i;
+      atomicOr(&dropped[(c1 - D + i) >> 5], 1u << ((c1 - D + i) & 31));
+    }
+    __syncwarp();
+  }
   if (!order_free) {
-    // kept slots ascending, run by run: slot s between drops r-1 and r goes to out[s - r]
-    for (int r = 0; r <= D; ++r) {
-      const int s0 = r == 0 ? 0 : drops[r - 1] + 1, s1 = r == D ? L : drops[r];
-      for (int s = s0 + lane; s < s1; s += 32) out[s - r] = s;
+    // kept slots ascending: a kept slot s goes to out[s - (dropped slots below s)],
+    // one word of the dropped-slot mask (32 slots, one per lane) per round
+    int below = 0;  // dropped slots in the words before w
+    for (int w = 0; w < words; ++w) {
+      const uint32_t bits = dropped[w];
+      const int s = w * 32 + lane;
+      if (s < L && !((bits >> lane) & 1u)) {
+        const int pos = s - below - __popc(bits & ((1u << lane) - 1u));
+        if (BKV_IN_RANGE(pos >= 0 && pos < budget, status)) out[pos] = s;
+      }
+      below += __popc(bits);
     }
   } else {
     // layout of the order-free compaction: slots below the budget keep their
@@ -245,10 +283,10 @@ __device__ bool select_keep(const float* sc, int L, int prefix, int recent, int 
     for (int k = lane; k < h; k += 32) {
       int x = budget + k;  // the k-th slot >= budget that is not dropped
       for (int r = h; r < D && drops[r] <= x; ++r) ++x;
-      out[drops[k]] = x;
+      if (BKV_IN_RANGE(drops[k] >= 0 && drops[k] < budget && x < L, status)) out[drops[k]] = x;
     }
   }
-  return bad;
+  return !consistent ? (uint32_t)BKV_ERR_INTERNAL : bad ? (uint32_t)BKV_ERR_NONFINITE : (uint32_t)BKV_OK;
 }
 
 // Miscellaneous shared memory: control word [0, 64), dropped-slot bitmask
@@ -274,12 +312,10 @@ struct Layout {
 // compacting in slot order, two chunks (and more K stages) for the order-free
 // compaction, which moves at most L - budget rows; two score buffers (one
 // when nothing else fits).
-__host__ __device__ inline Layout make_layout(int Rtot, int L, int nr, int budget, int compact) {
+__host__ __device__ inline Layout make_layout_chunks(int Rtot, int L, int nr, int budget, int compact, int chunks) {
   Layout s;
-  // more than 256 rows run as equal chunks (the last one padded with masked
-  // zero rows): two TMEM buffers of two M tiles hold 256 rows
   s.Rtot = Rtot;
-  s.chunks = (Rtot + 255) / 256 > 0 ? (Rtot + 255) / 256 : 1;
+  s.chunks = chunks;
   const int R = (Rtot + s.chunks - 1) / s.chunks;
   s.R = R;
   s.Rp16 = (R + 15) & ~15;
@@ -338,6 +374,26 @@ __host__ __device__ inline Layout make_layout(int Rtot, int L, int nr, int budge
   off += kMiscBytes;
   s.total = off + 1024;
   return s;
+}
+
+// More than 256 rows run as equal chunks (the last one padded with masked
+// zero rows): two TMEM buffers of two M tiles hold 256 rows. Between 129 and
+// 256 rows one chunk fits, but its rows (bf16 hi + lo) can leave the slot-
+// order compaction fewer than four 8 KB chunk buffers, and the copier, short
+// of bytes in flight, becomes the bound (R = 224 at budgets >= 1024: two
+// buffers). Such units are then scored in two chunks of half the rows: K is
+// read twice as often, but the freed shared memory gives the copier eight
+// buffers (measured on R1-Distill-Qwen-7B's shape, batch 128: budget 1024
+// 5.72 -> 4.72 ms, budget 4096 20.3 -> 17.8 ms; at budget 256, with four
+// buffers already, two chunks were slower).
+__host__ __device__ inline Layout make_layout(int Rtot, int L, int nr, int budget, int compact) {
+  const int chunks = (Rtot + 255) / 256 > 0 ? (Rtot + 255) / 256 : 1;
+  const Layout one = make_layout_chunks(Rtot, L, nr, budget, compact, chunks);
+  if (chunks == 1 && Rtot > 128 && compact == 1 && one.cbufs < 4) {
+    const Layout two = make_layout_chunks(Rtot, L, nr, budget, compact, 2);
+    if (two.stages >= 2 && two.cbufs > one.cbufs) return two;
+  }
+  return one;
 }
 
 }  // namespace
@@ -637,6 +693,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
                     const int n = end - crow < kChunkRows ? end - crow : kChunkRows;
                     c = make_int4(ct, crow, n, cr + 1);  // run cr moves down by cr + 1 slots
                     crow += n;
+                    // source rows inside the cache, destination rows inside the budget
+                    if (!BKV_IN_RANGE(c.y > c.w && c.y + c.z <= L && c.y - c.w + c.z <= P.budget, P.status))
+                      return false;
                     return true;
                   }
                   if (++cr < D) {
@@ -777,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
                 int r = drops_below(dl, s0), seg = s0;
                 for (;;) {
                   const int stop = r < D && dl[r] < end ? dl[r] : end;
-                  if (stop > seg)
+                  if (stop > seg && BKV_IN_RANGE(seg - r >= 0 && stop - r <= P.budget, P.status))
                     bulk_store(dst + (size_t)(seg - r) * (kD * 2), buf + (uint32_t)(seg - s0) * (kD * 2),
                                (uint32_t)(stop - seg) * (kD * 2), stream);
                   if (stop == end) break;
@@ -839,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
                 int x, rank;
                 const bool kept = slot(m, x, rank);
                 const int row = __popc(__ballot_sync(kFull, kept) & ((1u << lane) - 1u));
-                if (kept) {
+                if (kept && BKV_IN_RANGE(rank >= 0 && rank < h && dl[rank] < P.budget && x < L, P.status)) {
                   const int hole = dl[rank];
                   bulk_store(tk + (size_t)hole * (kD * 2),
                              smem_u32(cst + (size_t)(2 * set) * kChunkBytes + (size_t)row * (kD * 2)), kD * 2, stream);
@@ -907,10 +966,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       if (!ok) break;
       const int u = blockIdx.x + it * gridDim.x;
       const float* s_u = sc + (size_t)b * lay.Lp;
-      const bool bad = select_keep(s_u, L, P.prefix, P.recent, P.budget, P.kept + (size_t)u * P.budget,
-                                   dropbits, dlist + db * lay.D, P.compact == 2,
-                                   reinterpret_cast<int*>(smem + lay.misc + 2048));
-      if (bad && lane == 0) latch(P.status, BKV_ERR_NONFINITE);
+      const uint32_t code = select_keep(s_u, L, P.prefix, P.recent, P.budget, P.kept + (size_t)u * P.budget,
+                                        dropbits, dlist + db * lay.D, P.compact == 2,
+                                        reinterpret_cast<int*>(smem + lay.misc + 2048), P.status);
+      if (code != BKV_OK && lane == 0) latch(P.status, code);
       if (P.scores) {
         float* so = P.scores + (size_t)u * P.max_cache;
         for (int j = lane; j < L; j += 32) so[j] = s_u[j];
@@ -1076,6 +1135,11 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
                 float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
                 if (j < L) {
                   if (!first) mx = fmaxf(mx, s_u[j]);
+                  // every key is visible to the newest observation row, so a
+                  // log-weight of -inf on every row means a -inf logit: a
+                  // non-finite key (+inf and NaN keys give NaN scores, which
+                  // the selector reports)
+                  if (last && mx == neg_inf) latch(P.status, BKV_ERR_NONFINITE);
                   s_u[j] = !last ? mx : (mx == neg_inf ? 0.f : fast_exp2(mx));
                 }
               }
@@ -1193,7 +1257,7 @@ bool encode_kmaps(ScoreParams& p, const void* const* K, int layers, int batch, i
 cudaError_t launch_score_select(const ScoreParams& p, cudaStream_t s) {
   const int rows = p.group * (p.nb + p.nr);
   const size_t smem = score_smem_bytes(rows, p.L, p.nr, p.budget, p.compact);
-  const bool chunked = rows > 256;
+  const bool chunked = make_layout(rows, p.L, p.nr, p.budget, p.compact).chunks > 1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
