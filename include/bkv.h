@@ -242,7 +242,9 @@ bkv_status bkv_profile_read(bkv_handle h, bkv_kernel_times* out);
  * its one scratch buffer, the RoPE cos/sin table of the eviction step
  * (16,896 bytes), is a file-scope __device__ array that every GPU loading the
  * library holds until the process exits.
- *   cfg:      as bkv_create (flags ignored).
+ *   cfg:      as bkv_create. BKV_FLAG_MEAN_POOL selects mean pooling as in
+ *             bkv_evict; BKV_FLAG_KEEP_SCORES and BKV_FLAG_ORDER_FREE have no
+ *             effect (no scores are kept, nothing is compacted).
  *   bq:       device bf16 [layers][batch][heads][fps_cap][d]; rows [0, beacons)
  *             of each query head are its pre-RoPE beacons, oldest first.
  *   rq:       device bf16 [layers][batch][heads][fps_cap - fps_keep][d]; the
@@ -250,21 +252,29 @@ bkv_status bkv_profile_read(bkv_handle h, bkv_kernel_times* out);
  *             step tau in slot tau % (fps_cap - fps_keep).
  *   beacons:  0 <= beacons < fps_cap; recents: 0 <= recents <= fps_cap - fps_keep
  *             and at most 32 (BKV_ERR_UNSUPPORTED beyond: the scratch holds
- *             1 + 32 table rows).
+ *             1 + 32 table rows); beacons + recents >= 1.
  *   K, cache_len, step, kept: as bkv_evict, but cache_len is only checked
  *             against budget < cache_len <= max_cache. Nothing else is written:
  *             no compaction, no FPS, no state.
+ *   status:   optional device uint32 (4-byte aligned, caller-owned). The call
+ *             sets it to 0, then the kernel latches the first device-side
+ *             error: BKV_ERR_TIMEOUT (a bounded wait ran out; kept is then
+ *             partly unwritten and must not be used), BKV_ERR_NONFINITE (a
+ *             score was NaN, e.g. from a non-finite key). NULL: such errors go
+ *             unreported, and a timeout cannot be told from success.
  *   cuda_stream: where the work is enqueued.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture. Every call rewrites the whole table before using
- * it; calls whose work overlaps on the GPU share the array and race, so order
- * them. Device-side conditions (non-finite scores) are not reported here;
- * host checks return BKV_ERR_INVALID_ARG / BKV_ERR_UNSUPPORTED / BKV_ERR_CUDA. */
+ * before any stream capture. The address is kept for later calls, so do not
+ * call this entry point on a device after resetting it (cudaDeviceReset).
+ * Every call rewrites the whole table before using it; calls whose work
+ * overlaps on the GPU share the array and race, so order them. Host checks
+ * return BKV_ERR_INVALID_ARG / BKV_ERR_UNSUPPORTED / BKV_ERR_CUDA and
+ * enqueue nothing. */
 bkv_status bkv_score_select_noalloc(const bkv_config* cfg, const void* bq, const void* rq,
                                     int32_t beacons, int32_t recents, void* const* K,
                                     int32_t cache_len, int64_t step, int32_t* kept,
-                                    void* cuda_stream);
+                                    uint32_t* status, void* cuda_stream);
 
 /* Self-test of the bounded device-side waits every kernel uses (the timeout
  * latch and the abort of the other waiting warps): enqueues on the handle's

@@ -15,9 +15,15 @@ from dataclasses import dataclass
 
 import numpy as np
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libbkv.so")
+# BKV_LIBRARY=checked loads the bounds-checked build (libbkv_checked.so)
+_VARIANTS = {"": "libbkv.so", "checked": "libbkv_checked.so"}
+_variant = os.environ.get("BKV_LIBRARY", "")
+if _variant not in _VARIANTS:
+    raise ImportError(f"BKV_LIBRARY={_variant!r}: expected one of {sorted(_VARIANTS)}")
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), _VARIANTS[_variant])
 if not os.path.exists(_LIB_PATH):
-    raise ImportError(f"{_LIB_PATH} is missing: build it with kv_cache_eviction_head_gb300.build.build()")
+    raise ImportError(f"{_LIB_PATH} is missing: build it with kv_cache_eviction_head_gb300.build.build()"
+                      + (" (checked=True)" if _variant else ""))
 _lib = ctypes.CDLL(_LIB_PATH)
 
 BKV_OK = 0
@@ -77,7 +83,7 @@ _lib.bkv_get_stats.argtypes = [_vp, ctypes.POINTER(BkvStats)]
 _lib.bkv_profile.argtypes = [_vp, _i32]
 _lib.bkv_profile_read.argtypes = [_vp, ctypes.POINTER(BkvKernelTimes)]
 _lib.bkv_score_select_noalloc.argtypes = [ctypes.POINTER(BkvConfig), _vp, _vp, _i32, _i32,
-                                          ctypes.POINTER(_vp), _i32, _i64, _vp, _vp]
+                                          ctypes.POINTER(_vp), _i32, _i64, _vp, _vp, _vp]
 _lib.bkv_destroy.argtypes = [_vp]
 _lib.bkv_destroy.restype = None
 _lib.bkv_status_str.argtypes = [_i32]
@@ -99,6 +105,26 @@ def bkv_status_str(code: int) -> str:
 def _check(code: int, where: str) -> None:
     if code != BKV_OK:
         raise BkvError(code, where)
+
+
+def _check_tensor(t, name: str, dtype, shape) -> None:
+    """Raises ValueError unless t is a contiguous CUDA tensor of this dtype and shape."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor of shape {tuple(shape)}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device}"
+                         f"{'' if t.is_contiguous() else ' (not contiguous)'}")
+
+
+def _check_layers(ts, name: str, cfg) -> None:
+    """`layers` bf16 caches [batch][kv_heads][max_cache][d], one per layer."""
+    import torch
+    if len(ts) != cfg.layers:
+        raise ValueError(f"{name}: expected {cfg.layers} per-layer tensors, got {len(ts)}")
+    for l, t in enumerate(ts):
+        _check_tensor(t, f"{name}[{l}]", torch.bfloat16, (cfg.batch, cfg.kv_heads, cfg.max_cache, cfg.d))
 
 
 def _stream_ptr(stream) -> int:
@@ -142,12 +168,20 @@ def bkv_set_stream(h: Handle, stream) -> None:
 
 def bkv_append_queries(h: Handle, q_pre, step: int) -> None:
     """q_pre: bf16 CUDA tensor [layers][batch][heads][d], contiguous."""
+    import torch
+    c = h.cfg
+    _check_tensor(q_pre, "q_pre", torch.bfloat16, (c.layers, c.batch, c.heads, c.d))
     _check(_lib.bkv_append_queries(_vp(h.ptr), _vp(q_pre.data_ptr()), _i64(step)), "bkv_append_queries")
 
 
 def bkv_evict(h: Handle, K, V, cache_len: int, step: int, kept) -> None:
     """K, V: sequences of `layers` bf16 CUDA tensors [batch][kv_heads][max_cache][d];
     kept: int32 CUDA tensor [layers][batch][kv_heads][budget]."""
+    import torch
+    c = h.cfg
+    _check_layers(K, "K", c)
+    _check_layers(V, "V", c)
+    _check_tensor(kept, "kept", torch.int32, (c.layers, c.batch, c.kv_heads, c.budget))
     n = len(K)
     kp = (_vp * n)(*[t.data_ptr() for t in K])
     vp = (_vp * n)(*[t.data_ptr() for t in V])
@@ -164,6 +198,14 @@ def bkv_evict_ptrs(h: Handle, kptrs, vptrs, cache_len: int, step: int, kept_ptr:
 def bkv_prefill(h: Handle, q_prompt, first_step: int, trace_out=None) -> None:
     """q_prompt: bf16 CUDA tensor [P][layers][batch][heads][d]; trace_out: optional
     int32 CUDA tensor [layers][batch][heads][min(fps_keep, P - recents)]."""
+    import torch
+    c = h.cfg
+    P = q_prompt.shape[0] if q_prompt.dim() == 5 else -1
+    _check_tensor(q_prompt, "q_prompt", torch.bfloat16, (P, c.layers, c.batch, c.heads, c.d))
+    if trace_out is not None:
+        n_rq = c.fps_cap - c.fps_keep
+        m = min(c.fps_keep, P - min(n_rq, P))
+        _check_tensor(trace_out, "trace_out", torch.int32, (c.layers, c.batch, c.heads, m))
     _check(_lib.bkv_prefill(_vp(h.ptr), _vp(q_prompt.data_ptr()), _i32(q_prompt.shape[0]),
                             _i64(first_step), _vp(trace_out.data_ptr() if trace_out is not None else 0)),
            "bkv_prefill")
@@ -172,6 +214,11 @@ def bkv_prefill(h: Handle, q_prompt, first_step: int, trace_out=None) -> None:
 def bkv_coverage(h: Handle, q_future, out) -> None:
     """q_future: bf16 CUDA tensor [n_future][layers][batch][heads][d];
     out: float64 CUDA tensor [layers][batch][heads][n_future]."""
+    import torch
+    c = h.cfg
+    n = q_future.shape[0] if q_future.dim() == 5 else -1
+    _check_tensor(q_future, "q_future", torch.bfloat16, (n, c.layers, c.batch, c.heads, c.d))
+    _check_tensor(out, "out", torch.float64, (c.layers, c.batch, c.heads, n))
     _check(_lib.bkv_coverage(_vp(h.ptr), _vp(q_future.data_ptr()), _i32(q_future.shape[0]),
                              _vp(out.data_ptr())), "bkv_coverage")
 
@@ -220,15 +267,29 @@ def bkv_profile_read(h: Handle) -> dict:
 
 
 def bkv_score_select_noalloc(cfg: BkvConfig, bq, rq, beacons: int, recents: int, K,
-                             cache_len: int, step: int, kept, stream=None) -> None:
+                             cache_len: int, step: int, kept, status=None, stream=None) -> None:
     """Score + keep-set selection without a handle or workspace (see include/bkv.h).
-    bq, rq: bf16 CUDA tensors in the state layout; K: `layers` bf16 CUDA tensors;
-    kept: int32 CUDA tensor [layers][batch][kv_heads][budget]."""
+    bq: bf16 CUDA tensor [layers][batch][heads][fps_cap][d]; rq: bf16 CUDA tensor
+    [layers][batch][heads][fps_cap - fps_keep][d]; K: `layers` bf16 CUDA tensors
+    [batch][kv_heads][max_cache][d]; kept: int32 CUDA tensor
+    [layers][batch][kv_heads][budget]; status: optional uint32-sized CUDA tensor
+    (int32, one element) receiving the device-side status."""
+    import torch
+    c = cfg
+    n_rq = c.fps_cap - c.fps_keep
+    _check_tensor(bq, "bq", torch.bfloat16, (c.layers, c.batch, c.heads, c.fps_cap, c.d))
+    _check_tensor(rq, "rq", torch.bfloat16, (c.layers, c.batch, c.heads, n_rq, c.d))
+    _check_layers(K, "K", c)
+    _check_tensor(kept, "kept", torch.int32, (c.layers, c.batch, c.kv_heads, c.budget))
+    if status is not None:
+        _check_tensor(status, "status", torch.int32, (1,))
     n = len(K)
     kp = (_vp * n)(*[t.data_ptr() for t in K])
     _check(_lib.bkv_score_select_noalloc(ctypes.byref(cfg), _vp(bq.data_ptr()), _vp(rq.data_ptr()),
                                          _i32(beacons), _i32(recents), kp, _i32(cache_len),
-                                         _i64(step), _vp(kept.data_ptr()), _vp(_stream_ptr(stream))),
+                                         _i64(step), _vp(kept.data_ptr()),
+                                         _vp(status.data_ptr() if status is not None else 0),
+                                         _vp(_stream_ptr(stream))),
            "bkv_score_select_noalloc")
 
 

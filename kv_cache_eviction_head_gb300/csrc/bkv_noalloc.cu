@@ -15,7 +15,14 @@
 // the process exits. All calls on a device share it and each call overwrites
 // it completely before use, so nothing has to start zeroed; calls whose work
 // overlaps on the GPU (different streams, no ordering between them) race on
-// it and must be ordered by the caller.
+// it and must be ordered by the caller. The array's device address is looked
+// up once per device and kept; a device reset (cudaDeviceReset) may move it,
+// so a process that resets a device must not call this entry point on that
+// device again.
+//
+// Device-side failures (a bounded wait that ran out, a non-finite score) are
+// latched into the caller's optional status word, which the call zeroes
+// first; without one they go unreported.
 #include <mutex>
 
 #include "bkv_internal.cuh"
@@ -58,8 +65,9 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 extern "C" bkv_status bkv_score_select_noalloc(const bkv_config* c, const void* bq, const void* rq,
                                                int32_t beacons, int32_t recents, void* const* K,
                                                int32_t cache_len, int64_t step, int32_t* kept,
-                                               void* cuda_stream) {
+                                               uint32_t* status, void* cuda_stream) {
   if (!c || !bq || !rq || !K || !kept) return BKV_ERR_INVALID_ARG;
+  if (c->flags & ~(BKV_FLAG_KEEP_SCORES | BKV_FLAG_ORDER_FREE | BKV_FLAG_MEAN_POOL)) return BKV_ERR_INVALID_ARG;
   if (c->heads <= 0 || c->kv_heads <= 0 || c->heads % c->kv_heads != 0 || c->budget <= 0 ||
       c->prefix < 0 || c->recent < 0 || (int64_t)c->prefix + c->recent > c->budget ||
       c->fps_cap <= 0 || c->fps_keep < 0 || c->fps_keep >= c->fps_cap || c->layers <= 0 ||
@@ -68,10 +76,10 @@ extern "C" bkv_status bkv_score_select_noalloc(const bkv_config* c, const void* 
   if (c->d != bkv::kD || c->fps_cap > bkv::kMaxFpsCap || c->layers > bkv::kMaxLayers)
     return BKV_ERR_UNSUPPORTED;
   const int n_rq = c->fps_cap - c->fps_keep;
-  if (beacons < 0 || beacons >= c->fps_cap || recents < 0 || recents > n_rq)
-    return BKV_ERR_INVALID_ARG;
+  if (beacons < 0 || beacons >= c->fps_cap || recents < 0 || recents > n_rq || beacons + recents == 0)
+    return BKV_ERR_INVALID_ARG;  // no observation row: nothing to score with
   if (recents > kMaxRecents) return BKV_ERR_UNSUPPORTED;  // scratch holds 1 + 32 RoPE rows
-  if (!aligned(bq, 16) || !aligned(rq, 16) || !aligned(kept, 4)) return BKV_ERR_INVALID_ARG;
+  if (!aligned(bq, 16) || !aligned(rq, 16) || !aligned(kept, 4) || !aligned(status, 4)) return BKV_ERR_INVALID_ARG;
   for (int l = 0; l < c->layers; ++l)
     if (!K[l] || !aligned(K[l], 16)) return BKV_ERR_INVALID_ARG;
   if (cache_len <= c->budget || cache_len > c->max_cache || step < recents - 1)
@@ -86,6 +94,7 @@ extern "C" bkv_status bkv_score_select_noalloc(const bkv_config* c, const void* 
   float2* scratch = nullptr;
   if (scratch_for_current_device(&scratch) != cudaSuccess) return BKV_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  if (status && cudaMemsetAsync(status, 0, sizeof(uint32_t), s) != cudaSuccess) return BKV_ERR_CUDA;
 
   bkv::RopeParams rp{};
   rp.tab = scratch;
@@ -101,7 +110,7 @@ extern "C" bkv_status bkv_score_select_noalloc(const bkv_config* c, const void* 
   if (!bkv::encode_kmaps(sp, K, c->layers, c->batch, c->kv_heads, c->max_cache)) return BKV_ERR_CUDA;
   sp.kept = kept;
   sp.scores = nullptr;
-  sp.status = nullptr;
+  sp.status = status;  // may be null: device errors then go unreported
   sp.batch = c->batch;
   sp.kv_heads = c->kv_heads;
   sp.group = group;
@@ -117,6 +126,7 @@ extern "C" bkv_status bkv_score_select_noalloc(const bkv_config* c, const void* 
   sp.max_cache = c->max_cache;
   sp.units = (int)units;
   sp.compact = 0;  // score and keep set only
+  sp.pool_mean = (c->flags & BKV_FLAG_MEAN_POOL) ? 1 : 0;
   if (bkv::launch_score_select(sp, s) != cudaSuccess) return BKV_ERR_CUDA;
   return BKV_OK;
 }

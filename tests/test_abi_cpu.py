@@ -100,3 +100,30 @@ def test_status_strings(bkv):
     assert bkv.bkv_status_str(0) == "BKV_OK"
     assert bkv.bkv_status_str(5) == "BKV_ERR_NONFINITE"
     assert bkv.bkv_status_str(99) == "BKV_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("over,beacons,recents,cache_len,status,code", [
+    (dict(), 16, 16, 2064, 0, 0),            # valid: would launch, not run here
+    (dict(), 16, 17, 2064, 0, 1),            # more recents than the ring holds
+    (dict(fps_keep=0), 0, 33, 2064, 0, 1),   # beyond the 32 recents of the static table
+    (dict(), 32, 0, 2064, 0, 1),             # beacons == fps_cap
+    (dict(), 0, 0, 2064, 0, 1),              # no observation row at all
+    (dict(), -1, 16, 2064, 0, 1),
+    (dict(flags=8), 16, 16, 2064, 0, 1),     # unknown flag
+    (dict(), 16, 16, 2048, 0, 1),            # cache_len not above the budget
+    (dict(), 16, 16, 2065, 0, 1),            # cache_len beyond max_cache
+    (dict(), 16, 16, 2064, 4096 + 2, 1),     # misaligned status word
+    (dict(d=64), 16, 16, 2064, 0, 7),
+    (dict(layers=129), 16, 16, 2064, 0, 7),
+])
+def test_noalloc_argument_checks_before_any_cuda_call(bkv, over, beacons, recents, cache_len, status, code):
+    """bkv_score_select_noalloc validates everything on the host and returns
+    the documented code before it touches the device (fake, aligned device
+    addresses are enough: nothing is dereferenced)."""
+    c = cfg_for(bkv, **{"layers": 2, "batch": 1, **over})
+    K = (ctypes.c_void_p * max(c.layers, 1))(*[4096 * (i + 1) for i in range(max(c.layers, 1))])
+    args = (ctypes.byref(c), ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20), beacons, recents, K,
+            cache_len, 5000, ctypes.c_void_p(3 << 20), ctypes.c_void_p(status), None)
+    if code == 0:
+        return  # the valid call would launch kernels: covered by the GPU tests
+    assert bkv.raw_status("bkv_score_select_noalloc", *args) == code
