@@ -10,12 +10,14 @@ exact-sum path.
 
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 import pytest
 import torch
 
 from synth import WORKLOADS
-from tests.lockstep import run_lockstep
+from tests.lockstep import run_lockstep, run_lockstep_parallel
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +56,9 @@ def test_tiny_full_stream():
     # 5 heads x (12..31 beacons + 16 recents): observation rows sweep 140..235,
     # so the second M tile starts at every 16-row offset past 128 (a split warp)
     ("gqa5_rows_sweep", dict(heads=5, kv_heads=1, fps_keep=12, steps=400)),
+    # 224 rows and a 1016-slot cache: the single-chunk plan leaves two
+    # compaction buffers, so the rows are scored in two chunks of 112
+    ("gqa7_two_row_chunks", dict(heads=7, kv_heads=1, budget=1000, steps=1100)),
 ])
 def test_tiny_variants(name, over):
     w = TINY.with_(**{"steps": 240, **over})
@@ -102,6 +107,48 @@ def test_qwen3_4b_b1_first_eviction_sampled_units():
     assert rep.units_checked == len(units) * rep.evictions
 
 
+def test_qwen3_4b_b1_every_unit():
+    """The Qwen3-4B single-sequence configuration: its one eviction over all
+    36 layers checked on every one of its 288 units (the oracles run in
+    parallel worker processes)."""
+    w = WORKLOADS["qwen3_4b_b1"]
+    rep = run_lockstep_parallel(w, seed=0xBEAC1, steps=w.budget + w.period)
+    assert_clean(rep)
+    assert rep.evictions == 1 and rep.units_checked == w.units == 288
+
+
+# Long horizon: each configuration's own stream length on its head shape, with a
+# small batch and layer count so that the oracles keep up; every unit checked at
+# every eviction (continual FPS across thousands of evictions, ring-slot and
+# trace arithmetic at large steps, RoPE angles at positions up to 32K).
+
+def test_long_horizon_r1_qwen7b_32768_steps():
+    """R1-Distill-Qwen-7B head shape (GQA 7, theta 1e4, budget 1024): the
+    full 32,768-step stream, 1,984 evictions per unit, 8 units."""
+    w = WORKLOADS["r1_qwen7b_b128_k1024"].with_(layers=1, batch=2)
+    rep = run_lockstep_parallel(w, seed=0xBEAF0, steps=32768)
+    assert_clean(rep, min_evictions=1984)
+    assert rep.units_checked == 8 * rep.evictions
+
+
+def test_long_horizon_qwen3_4b_4096_steps():
+    """Qwen3-4B head shape (budget 2048): the 4,096-step stream, 128 evictions
+    per unit, 2 layers x 2 sequences x 8 KV heads."""
+    w = WORKLOADS["qwen3_4b_b192"].with_(layers=2, batch=2)
+    rep = run_lockstep_parallel(w, seed=0xBEAF1, steps=4096)
+    assert_clean(rep, min_evictions=128)
+    assert rep.units_checked == 32 * rep.evictions
+
+
+def test_long_horizon_qwen3_14b_4096_steps():
+    """Qwen3-14B head shape (GQA 5, 8 centres, budget 1024): a 4,096-step
+    stream, 192 evictions per unit, 2 sequences x 8 KV heads."""
+    w = WORKLOADS["qwen3_14b_b64"].with_(layers=1, batch=2)
+    rep = run_lockstep_parallel(w, seed=0xBEAF2, steps=4096)
+    assert_clean(rep, min_evictions=192)
+    assert rep.units_checked == 16 * rep.evictions
+
+
 def test_qwen3_4b_b192_full_size_sampled_units():
     """The benchmark workload at full size (58 GB of K/V, 55,296 units, the
     bench's launch configuration), checked on sampled units over three
@@ -126,11 +173,11 @@ def test_qwen3_14b_b64_full_size_sampled_units():
     assert rep.units_checked == len(units) * rep.evictions
 
 
-@pytest.mark.parametrize("budget", [256, 1024, 4096])
+@pytest.mark.parametrize("budget", [256, 512, 1024, 2048, 4096])
 def test_r1_qwen7b_b128_full_size_sampled_units(budget):
     """R1-Distill-Qwen-7B head shape (GQA 7, 224 observation rows, theta 1e4)
-    at batch 128 over the budget sweep's small, middle and largest budgets:
-    full-size cache, three evictions, sampled units."""
+    at batch 128 over every budget of the sweep: full-size cache, three
+    evictions, sampled units."""
     w = WORKLOADS[f"r1_qwen7b_b128_k{budget}"]
     units = [(0, 0, 0), (27, 127, 3), (13, 64, 1), (5, 100, 2), (21, 7, 0)]
     rep = run_lockstep(w, seed=0xBEAC4 + budget, sample_units=units, gen_device="cuda",
@@ -417,9 +464,11 @@ def test_step_order_and_cache_length_are_validated():
         with pytest.raises(bkv.BkvError) as e:
             bkv.bkv_append_queries(h, q, 12)             # skipped a step
         assert e.value.code == bkv.BKV_ERR_STATE
-        with pytest.raises(bkv.BkvError) as e:
-            bkv.bkv_append_queries(h, torch.empty(513, dtype=torch.bfloat16, device=dev)[1:], 11)
-        assert e.value.code == bkv.BKV_ERR_INVALID_ARG   # misaligned pointer
+        bad = torch.empty(4 * 128 + 1, dtype=torch.bfloat16, device=dev)
+        assert bkv.raw_status("bkv_append_queries", ctypes.c_void_p(h.ptr),
+                              ctypes.c_void_p(bad.data_ptr() + 2), 11) == bkv.BKV_ERR_INVALID_ARG
+        with pytest.raises(ValueError):                  # the binding checks shapes first
+            bkv.bkv_append_queries(h, bad[1:], 11)
         for t in range(11, 11 + w.budget + 15):
             bkv.bkv_append_queries(h, q, t)
         last = 10 + w.budget + 15
