@@ -307,13 +307,22 @@ def run_ours(args, w):
     for p in range(n_periods):
         for i in range(w.period):
             qpool[p, i] = stream.queries()
+    # and the keys and values its decode steps append at slots [budget, L)
+    kvpool = torch.empty(n_periods, w.layers, 2, w.batch, w.kv_heads, w.period, w.d, dtype=torch.bfloat16,
+                         device=dev)
+    for p in range(n_periods):
+        fresh_tail(stream, w, kvpool[p], w.max_cache + p * w.period)
     bkv.bkv_sync(h)
     state = {"t": w.max_cache - 1, "p": 0}
 
     def step():
         t = state["t"]
         qper = qpool[state["p"] % n_periods]
+        tail = kvpool[state["p"] % n_periods]
         bkv.bkv_evict_ptrs(h, kptr, vptr, w.max_cache, t, kept.data_ptr())
+        # the period's decode steps write their keys and values into the freed slots
+        K_all[:, :, :, w.budget:w.max_cache].copy_(tail[:, 0])
+        V_all[:, :, :, w.budget:w.max_cache].copy_(tail[:, 1])
         for i in range(w.period):
             bkv.bkv_append_queries(h, qper[i], t + 1 + i)
         state["t"] = t + w.period
@@ -399,7 +408,7 @@ def run_ours(args, w):
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        del qpool
+        del qpool, kvpool
         e2e = run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, stream, state, dev, cs)
         e2e["elapsed_ms"] = max_over_ranks(e2e["elapsed_ms"], world, dev)
         e2e = {"value": aggregate(evictions_per_step * e2e["steps"], e2e["elapsed_ms"] / 1e3, world),
@@ -466,7 +475,8 @@ def run_ours(args, w):
                        "fps": f"{w.fps_cap}->{w.fps_keep}", "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (K/V cache %.1f GB)" % (
                            2 * w.layers * w.batch * w.kv_heads * w.max_cache * w.d * 2 / 1e9),
-                       "step": f"1 eviction + {w.period} query appends",
+                       "step": f"1 eviction + {w.period} query appends + the period's fresh K/V rows "
+                               f"written to slots [budget, L) (one device copy per tensor)",
                        "compaction": "order-free (holes filled from the kept tail)" if args.order_free
                        else "slot order (eq. 8)",
                        "pooling": args.pool},
@@ -490,6 +500,16 @@ def run_ours(args, w):
     return 0
 
 
+def fresh_tail(stream, w, out, pos0: int) -> None:
+    """The synthetic stream's keys and values of positions pos0 .. pos0 +
+    period - 1 (what a period's decode steps append to the cache), into
+    out [layers][2][batch][kv_heads][period][d]."""
+    for i in range(w.period):
+        k, v = stream.keys_values(pos0 + i)
+        out[:, 0, :, :, i] = k
+        out[:, 1, :, :, i] = v
+
+
 def e2e_plan(period_bytes: int, warmup: int, steps: int, host_cap_bytes: int):
     """(warm-up, timed) steps of the e2e run: one host period of queries per
     step, at least one warm-up step, and no more periods than host_cap_bytes
@@ -511,28 +531,33 @@ def run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, stream, state, dev,
     K/V rows move into the cache (a device copy) once the eviction that reads
     those slots is done.
 
-    Every step gets a period of fresh queries from the stream (a repeated
-    period would hand FPS exact duplicates), generated before the timed region
-    straight into pinned host memory. The pool is capped at host_cap_bytes; a
-    workload whose periods do not fit runs fewer e2e steps (one warm-up and at
-    least one timed), and the returned step count says so."""
+    Every step gets a period of fresh queries and fresh keys and values from
+    the stream (a repeated period would hand FPS exact duplicates and the
+    scoring the same rows again), generated before the timed region straight
+    into pinned host memory. The pool is capped at host_cap_bytes; a workload
+    whose periods do not fit runs fewer e2e steps (one warm-up and at least
+    one timed), and the returned step count says so."""
     import torch
-    per_period = w.period * w.layers * w.batch * w.heads * w.d * 2
-    warm, steps = e2e_plan(per_period, args.warmup, args.steps, host_cap_bytes)
+    q_bytes = w.period * w.layers * w.batch * w.heads * w.d * 2
+    kv_bytes = w.layers * 2 * w.batch * w.kv_heads * w.period * w.d * 2
+    warm, steps = e2e_plan(q_bytes + kv_bytes, args.warmup, args.steps, host_cap_bytes)
     total = warm + steps
     q_host = torch.empty(total, w.period, w.layers, w.batch, w.heads, w.d, dtype=torch.bfloat16,
                          pin_memory=True)
     for p in range(total):
         for i in range(w.period):
             q_host[p, i].copy_(stream.queries())
-    # the new K/V rows of a period, host side (per layer: small device temporaries)
-    tail = torch.empty(w.layers, 2, w.batch, w.kv_heads, w.period, w.d, dtype=torch.bfloat16, pin_memory=True)
-    for l in range(w.layers):
-        tail[l, 0].copy_(K_all[l, :, :, w.budget:w.max_cache])
-        tail[l, 1].copy_(V_all[l, :, :, w.budget:w.max_cache])
+    # the new K/V rows of each period, host side
+    tail_host = torch.empty(total, w.layers, 2, w.batch, w.kv_heads, w.period, w.d, dtype=torch.bfloat16,
+                            pin_memory=True)
+    tmp = torch.empty(tail_host.shape[1:], dtype=torch.bfloat16, device=dev)
+    for p in range(total):
+        fresh_tail(stream, w, tmp, state["t"] + 1 + p * w.period)
+        tail_host[p].copy_(tmp)
+    del tmp
     xs = torch.cuda.Stream(dev)
     qstage = [torch.empty(q_host.shape[1:], dtype=q_host.dtype, device=dev) for _ in range(2)]
-    tstage = [torch.empty(tail.shape, dtype=tail.dtype, device=dev) for _ in range(2)]
+    tstage = [torch.empty(tail_host.shape[1:], dtype=tail_host.dtype, device=dev) for _ in range(2)]
     kept_dev = [kept, torch.empty_like(kept)]
     kept_host = [torch.empty(kept.shape, dtype=kept.dtype).pin_memory() for _ in range(2)]
     ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("staged", "used", "evicted", "read")}
@@ -544,7 +569,7 @@ def run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, stream, state, dev,
             if k >= 2:
                 xs.wait_event(ev["used"][b])  # step k - 2 is done with this buffer
             qstage[b].copy_(q_host[k], non_blocking=True)
-            tstage[b].copy_(tail, non_blocking=True)
+            tstage[b].copy_(tail_host[k], non_blocking=True)
             ev["staged"][b].record(xs)
 
     def step(k):
@@ -584,7 +609,7 @@ def run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, stream, state, dev,
     torch.cuda.synchronize(dev)
     bkv.bkv_sync(h)
     return {"elapsed_ms": e0.elapsed_time(e1), "steps": steps,
-            "h2d": qstage[0].numel() * 2 + tail.numel() * 2, "d2h": kept_host[0].numel() * 4}
+            "h2d": qstage[0].numel() * 2 + tstage[0].numel() * 2, "d2h": kept_host[0].numel() * 4}
 
 
 def kernel_source_digest(kernel: str):
