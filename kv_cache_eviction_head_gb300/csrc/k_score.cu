@@ -61,79 +61,70 @@ namespace bkv {
 
 namespace {
 
-// Large drop counts (D > kRadixFrom): the D-th smallest score is found digit
-// by digit (four 8-bit radix passes over a 256-bin shared histogram of the
-// candidates that match the digits chosen so far); every candidate below it
-// is dropped, and among those equal to it the highest slots fill the rest.
-// Softmax weights share a few exponents, so the lanes of a warp mostly hit
-// the same bin: lanes with equal bins are grouped (match.any) and one of them
-// adds the group's count.
-constexpr int kRadixFrom = 32;
+// Large drop counts (D > kThresholdFrom): the D-th smallest candidate score x is
+// found by a binary search over the 32-bit patterns (scores >= 0 order like
+// their patterns) between the smallest and the largest, each step counting
+// over the warp the candidates whose pattern is <= the midpoint (a warp-wide
+// add per step). Up to 2048 candidates the lane's share stays in registers
+// (the selector warp has the kernel's register budget to itself); beyond, the
+// counts read shared memory. Every candidate below x is dropped, and among
+// those equal to x the highest slots fill the rest.
+constexpr int kThresholdFrom = 32;
+constexpr int kRegCands = 64;  // candidates per lane held in registers
 // Scores are weights in [0, 1]; NaN or +inf comes only from a non-finite
 // input (a +inf logit, for one, turns its row's log-sum-exp into NaN or -inf).
 constexpr float kInf = __builtin_huge_valf();
-__device__ bool radix_drop(const float* sc, int c0, int c1, int D, uint32_t* dropped, int* hist) {
+__device__ bool threshold_drop(const float* sc, int c0, int c1, int D, uint32_t* dropped) {
   const int lane = threadIdx.x & 31;
   bool bad = false;
-  for (int j = c0 + lane; j < c1; j += 32) bad |= !(sc[j] < kInf);  // NaN or +inf
-  uint32_t prefix = 0u, mask = 0u;
-  int rank = D;  // rank (1-based) of the threshold among candidates matching `prefix`
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = lane; i < 256; i += 32) hist[i] = 0;
-    __syncwarp();
-    for (int j0 = c0; j0 < c1; j0 += 32) {
-      const int j = j0 + lane;
-      const uint32_t bits = j < c1 ? __float_as_uint(sc[j]) : 0u;
-      const bool take = j < c1 && (bits & mask) == prefix;
-      const unsigned act = __ballot_sync(kFull, take);
-      if (take) {
-        const uint32_t bin = (bits >> shift) & 0xFFu;
-        const unsigned same = __match_any_sync(act, bin);
-        if ((same & ((1u << lane) - 1u)) == 0u) atomicAdd(&hist[bin], __popc(same));
-      }
-    }
-    __syncwarp();
-    // lane l owns bins [8l, 8l + 8): the digit where the running count reaches rank
-    int cnt[8], sum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      cnt[i] = hist[8 * lane + i];
-      sum += cnt[i];
-    }
-    int incl = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(kFull, incl, off);
-      if (lane >= off) incl += y;
-    }
-    const int excl = incl - sum;
-    const unsigned owner = __ballot_sync(kFull, excl < rank && rank <= incl);
-    const int src = __ffs(owner) - 1;
-    int digit = 0, below = 0;
-    if (lane == src) {
-      int run = excl;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (run + cnt[i] >= rank) {
-          digit = 8 * lane + i;
-          below = run;
-          break;
-        }
-        run += cnt[i];
-      }
-    }
-    digit = __shfl_sync(kFull, digit, src);
-    below = __shfl_sync(kFull, below, src);
-    rank -= below;
-    prefix |= (uint32_t)digit << shift;
-    mask |= 0xFFu << shift;
-    __syncwarp();
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+  for (int j = c0 + lane; j < c1; j += 32) {
+    const float v = sc[j];
+    bad |= !(v < kInf);  // NaN or +inf
+    mn = min(mn, __float_as_uint(v));
+    mx = max(mx, __float_as_uint(v));
   }
-  // drop every candidate below the threshold, then `rank` of those equal to it,
-  // highest slots first
+  // smallest x with #(patterns <= x) >= D lies in [lo, hi]; every midpoint is
+  // below hi, so padding patterns of 0xFFFFFFFF are never counted
+  uint32_t lo = __reduce_min_sync(kFull, mn), hi = __reduce_max_sync(kFull, mx);
+  if (c1 - c0 <= 32 * kRegCands) {
+    uint32_t v[kRegCands];
+#pragma unroll
+    for (int k = 0; k < kRegCands; ++k) {
+      const int j = c0 + lane + 32 * k;
+      v[k] = j < c1 ? __float_as_uint(sc[j]) : 0xFFFFFFFFu;
+    }
+    while (lo < hi) {
+      const uint32_t mid = lo + ((hi - lo) >> 1);
+      int c = 0;
+#pragma unroll
+      for (int k = 0; k < kRegCands; ++k) c += v[k] <= mid ? 1 : 0;
+      if (__reduce_add_sync(kFull, c) >= D)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+  } else {
+    while (lo < hi) {
+      const uint32_t mid = lo + ((hi - lo) >> 1);
+      int c = 0;
+      for (int j = c0 + lane; j < c1; j += 32) c += __float_as_uint(sc[j]) <= mid ? 1 : 0;
+      if (__reduce_add_sync(kFull, c) >= D)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+  }
+  const uint32_t prefix = lo;  // the D-th smallest pattern
+  // drop every candidate below the threshold, then those equal to it still
+  // needed, highest slots first
+  int below = 0;
   for (int j = c0 + lane; j < c1; j += 32)
-    if (__float_as_uint(sc[j]) < prefix) atomicOr(&dropped[j >> 5], 1u << (j & 31));
-  int need = rank;
+    if (__float_as_uint(sc[j]) < prefix) {
+      atomicOr(&dropped[j >> 5], 1u << (j & 31));
+      ++below;
+    }
+  int need = D - __reduce_add_sync(kFull, below);
   for (int top = c1 - 1; top >= c0 && need > 0; top -= 32) {
     const int j = top - lane;  // lane 0 takes the highest slot of the chunk
     const bool tie = j >= c0 && __float_as_uint(sc[j]) == prefix;
@@ -213,7 +204,7 @@ __device__ bool list_drop(const float* sc, int c0, int c1, int D, uint32_t* drop
 // slots; drops[] then holds the D highest candidates instead, so that
 // everything downstream stays in bounds.
 __device__ uint32_t select_keep(const float* sc, int L, int prefix, int recent, int budget, int32_t* out,
-                                uint32_t* dropped, int* drops, bool order_free, int* hist, uint32_t* status) {
+                                uint32_t* dropped, int* drops, bool order_free, uint32_t* status) {
   static_assert(kList == 8, "the list networks are written for 8 keys");
   const int lane = threadIdx.x & 31;
   const int c0 = prefix < L ? prefix : L;
@@ -221,7 +212,7 @@ __device__ uint32_t select_keep(const float* sc, int L, int prefix, int recent, 
   const int D = L - budget;
   for (int wd = lane; wd < (L + 31) / 32; wd += 32) dropped[wd] = 0u;
   __syncwarp();
-  const bool bad = D > kRadixFrom ? radix_drop(sc, c0, c1, D, dropped, hist) : list_drop(sc, c0, c1, D, dropped);
+  const bool bad = D > kThresholdFrom ? threshold_drop(sc, c0, c1, D, dropped) : list_drop(sc, c0, c1, D, dropped);
   __syncwarp();
   // dropped slots ascending: per-word counts, a warp prefix sum, then the bits
   const int words = (L + 31) / 32;
@@ -290,9 +281,8 @@ __device__ uint32_t select_keep(const float* sc, int L, int prefix, int recent, 
 }
 
 // Miscellaneous shared memory: control word [0, 64), dropped-slot bitmask
-// [64, 1088) (L <= 8192), copier chunk descriptors [1536, 1664), radix
-// histogram of the selector [2048, 3072).
-constexpr int kMiscBytes = 3072;
+// [64, 1088) (L <= 8192), copier chunk descriptors [1536, 1664).
+constexpr int kMiscBytes = 1664;
 constexpr int kChunkRows = 32;                   // rows per compaction chunk
 constexpr int kChunkBytes = kChunkRows * kD * 2;  // 8 KB
 constexpr int kPfChunks = 16;                     // L2 prefetch lead of the copier in windows (few chunk buffers only)
@@ -967,8 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       const int u = blockIdx.x + it * gridDim.x;
       const float* s_u = sc + (size_t)b * lay.Lp;
       const uint32_t code = select_keep(s_u, L, P.prefix, P.recent, P.budget, P.kept + (size_t)u * P.budget,
-                                        dropbits, dlist + db * lay.D, P.compact == 2,
-                                        reinterpret_cast<int*>(smem + lay.misc + 2048), P.status);
+                                        dropbits, dlist + db * lay.D, P.compact == 2, P.status);
       if (code != BKV_OK && lane == 0) latch(P.status, code);
       if (P.scores) {
         float* so = P.scores + (size_t)u * P.max_cache;
