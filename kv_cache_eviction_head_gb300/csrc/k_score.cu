@@ -299,9 +299,10 @@ struct Layout {
 // lo), the per-row statistics and tables; the rest goes to K-tile stages,
 // compaction chunks and score buffers, in the first arrangement that fits:
 // two or more K stages always, eight / four / two 8 KB compaction chunks when
-// compacting in slot order, two chunks (and more K stages) for the order-free
-// compaction, which moves at most L - budget rows; two score buffers (one
-// when nothing else fits).
+// compacting in slot order (three stages and four chunks first for units
+// split into two row chunks, whose passes read K twice as often), two chunks
+// (and more K stages) for the order-free compaction, which moves at most
+// L - budget rows; two score buffers (one when nothing else fits).
 __host__ __device__ inline Layout make_layout_chunks(int Rtot, int L, int nr, int budget, int compact, int chunks) {
   Layout s;
   s.Rtot = Rtot;
@@ -323,12 +324,13 @@ __host__ __device__ inline Layout make_layout_chunks(int Rtot, int L, int nr, in
   const size_t scb = (size_t)s.Lp * 4;
   static const int plans[][3] = {{4, 0, 2}, {3, 0, 2}, {2, 0, 2}, {2, 0, 1}};          // no compaction
   static const int cplans[][3] = {{2, 8, 2}, {2, 4, 2}, {2, 2, 2}, {2, 2, 1}};         // compaction
+  static const int splans[][3] = {{3, 4, 2}, {2, 8, 2}, {2, 4, 2}, {2, 2, 1}};         // split units
   static const int oplans[][3] = {{4, 2, 2}, {3, 2, 2}, {2, 2, 2}, {2, 2, 1}};         // order-free
   s.stages = 0;
   s.cbufs = 0;
   s.scbufs = 0;
   for (int i = 0; i < 4; ++i) {
-    const int* pl = compact == 2 ? oplans[i] : compact ? cplans[i] : plans[i];
+    const int* pl = compact == 2 ? oplans[i] : compact ? (chunks == 2 && Rtot <= 256 ? splans[i] : cplans[i]) : plans[i];
     const size_t need = 2 * qbytes + (size_t)pl[0] * kTileBytes + (size_t)pl[1] * kChunkBytes + pl[2] * scb + small;
     if (need <= cap) {
       s.stages = pl[0];
