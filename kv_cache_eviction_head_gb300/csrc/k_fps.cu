@@ -14,13 +14,15 @@
 // pick this kernel makes is the pick that arithmetic makes, bit for bit, but
 // float64 runs only where it can change the answer:
 //   * each row is scaled by a power of two that brings its largest component
-//     into [1, 4), or above 2^-7 for a row of bf16 subnormals (exact, apart
-//     from components more than ~120 binades below the largest, which may
-//     round in the float32 subnormal range);
+//     into [1, 4), or above 2^-7 for a row of bf16 subnormals, and kept in
+//     shared memory as bf16 (exact, apart from components more than 126
+//     binades below the largest, which round to the bf16 subnormal grid with
+//     an error below 2^-134);
 //   * the float32 Gram entry is two interleaved sums (even and odd k) of 64
-//     exact bf16 products each, added once, so its error is at most
-//     gamma_64 * ||y_i|| ||y_j|| (3.8e-6 relative) plus < 2^-140 from
-//     subnormal rounding, against ||y_i|| >= 2^-7 for every nonzero row;
+//     bf16 products each (exact, or below 2^-149 off where a product
+//     underflows), added once, so its error is at most
+//     gamma_64 * ||y_i|| ||y_j|| (3.8e-6 relative) plus < 2^-123 from the
+//     subnormal roundings, against ||y_i|| >= 2^-7 for every nonzero row;
 //   * c_ij = (G32_ij * r_i) * r_j with r_i = rsqrtf(G32_ii) (2 ulp) is then
 //     within 8.5e-6 of the float64 cosine; the filters use kCosErr = 2e-5;
 //   * the mean a_i in float32 (any summation order, N <= 64) is within
@@ -48,7 +50,7 @@ namespace {
 
 constexpr int kHeadsPerCta = 2;       // one warp per head
 constexpr int kMaxCand = 64;          // beacons (< fps_cap <= 32) + recents (<= 32)
-constexpr int kYStride = kD + 4;      // float row stride: LDS.128 of 8 consecutive rows hit distinct banks
+constexpr int kYStride = kD + 8;      // bf16 row stride (272 bytes): 16-byte aligned rows, and LDS.64 of 8 consecutive rows hit distinct banks
 constexpr float kCosErr = 2e-5f;      // |c32 - cos64| bound used by the filters
 constexpr float kMeanErr = 2.5e-5f;   // |a32 - a64| bound used by the filters
 constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -57,13 +59,14 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 template <int NH>
 struct WarpSmem {
   static constexpr int NT = 32 * NH;
-  static constexpr size_t kY = (size_t)NT * kYStride * 4;
+  static constexpr size_t kY = (((size_t)NT * kYStride * 2 + 15) / 16) * 16;
   // NH == 1: the cosine matrix reuses the rows' space once the Gram is in registers
   static constexpr size_t kC = NH == 1 ? 0 : (((size_t)NT * (NT + 1) * 4 + 15) / 16) * 16;
+  static_assert(NH != 1 || (size_t)NT * (NT + 1) * 4 <= kY, "the cosine matrix fits in the rows' space");
   static constexpr size_t kMisc = (size_t)NT * 8 * 2 + (size_t)NT * 4 * 5 + 64 * 4;
   static constexpr size_t kBytes = ((kY + kC + kMisc) + 15) / 16 * 16;
 
-  float* y;       // [NT][kYStride] rows scaled by a power of two, float32
+  __nv_bfloat16* y;  // [NT][kYStride] rows scaled by a power of two, bf16 (exact, see the header)
   float* c;       // [NT][NT + 1]   Gram, then cosines
   double* diag;   // [NT] exact G_ii rounded to float64 (close calls only)
   double* v64;    // [NT] exact values of a close call
@@ -76,8 +79,8 @@ struct WarpSmem {
   int* keep_src;  // [32]
 
   __device__ WarpSmem(unsigned char* base) {
-    y = reinterpret_cast<float*>(base);
-    c = NH == 1 ? y : reinterpret_cast<float*>(base + kY);
+    y = reinterpret_cast<__nv_bfloat16*>(base);
+    c = NH == 1 ? reinterpret_cast<float*>(base) : reinterpret_cast<float*>(base + kY);
     unsigned char* m = base + kY + kC;
     diag = reinterpret_cast<double*>(m);
     v64 = diag + NT;
@@ -147,7 +150,7 @@ __device__ __forceinline__ int filtered_argmin(int* cand, float v0, float v1, bo
 }
 
 template <int NH>
-__global__ void __launch_bounds__(32 * kHeadsPerCta, 6) fps_kernel(FpsParams P) {
+__global__ void __launch_bounds__(32 * kHeadsPerCta, 8) fps_kernel(FpsParams P) {
   using W = WarpSmem<NH>;
   constexpr int NT = W::NT;
   extern __shared__ __align__(16) unsigned char fps_smem[];
@@ -191,15 +194,15 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta, 6) fps_kernel(FpsParams P) 
         for (int off = 1; off < 16; off <<= 1) e = max(e, __shfl_xor_sync(kFull, e, off));
         bad |= e == 0xFFu;
         const float scale = __int_as_float(max(254 - (int)e, 1) << 23);  // 2^(127 - e)
-        float f[8];
+        uint32_t o[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          f[2 * q] = __fmul_rn(__uint_as_float(w[q] << 16), scale);
-          f[2 * q + 1] = __fmul_rn(__uint_as_float(w[q] & 0xFFFF0000u), scale);
+          const float lo = __fmul_rn(__uint_as_float(w[q] << 16), scale);
+          const float hi = __fmul_rn(__uint_as_float(w[q] & 0xFFFF0000u), scale);
+          o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+                 ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
         }
-        float4* dst = reinterpret_cast<float4*>(sm.y + r * kYStride + part * 8);
-        dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-        dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+        *reinterpret_cast<uint4*>(sm.y + r * kYStride + part * 8) = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
     if (__any_sync(kFull, bad) && lane == 0) latch(P.status, BKV_ERR_NONFINITE);
@@ -212,8 +215,10 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta, 6) fps_kernel(FpsParams P) 
 #pragma unroll 1
     for (int tile = 0; tile < (NH == 1 ? 1 : 3); ++tile) {
       const int ti = tile == 2 ? 1 : 0, tj = tile == 0 ? 0 : 1;
-      const float* ya = sm.y + (ti * 32 + I) * kYStride;
-      const float* yb = sm.y + (tj * 32 + J) * kYStride;
+      const __nv_bfloat16* ya = sm.y + (ti * 32 + I) * kYStride;
+      const __nv_bfloat16* yb = sm.y + (tj * 32 + J) * kYStride;
+      // bf16 pair (k, k + 1) in one word -> float2 (exact)
+      auto pair = [](uint32_t w) { return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)); };
       float2 s[4][8];
 #pragma unroll
       for (int a = 0; a < 4; ++a)
@@ -221,19 +226,27 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta, 6) fps_kernel(FpsParams P) 
         for (int b = 0; b < 8; ++b) s[a][b] = make_float2(0.f, 0.f);
 #pragma unroll 2
       for (int k = 0; k < kD; k += 4) {
-        float4 av[4], bv[8];
+        uint2 av[4], bv[8];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) av[a] = *reinterpret_cast<const float4*>(ya + 8 * a * kYStride + k);
+        for (int a = 0; a < 4; ++a) av[a] = *reinterpret_cast<const uint2*>(ya + 8 * a * kYStride + k);
 #pragma unroll
-        for (int b = 0; b < 8; ++b) bv[b] = *reinterpret_cast<const float4*>(yb + 4 * b * kYStride + k);
+        for (int b = 0; b < 8; ++b) bv[b] = *reinterpret_cast<const uint2*>(yb + 4 * b * kYStride + k);
+        float2 b01[8], b23[8];
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int b = 0; b < 8; ++b) {
+          b01[b] = pair(bv[b].x);
+          b23[b] = pair(bv[b].y);
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const float2 a01 = pair(av[a].x), a23 = pair(av[a].y);
 #pragma unroll
           for (int b = 0; b < 8; ++b) {
             // (even k, odd k) partial sums of the same entry
-            s[a][b] = __ffma2_rn(make_float2(av[a].x, av[a].y), make_float2(bv[b].x, bv[b].y), s[a][b]);
-            s[a][b] = __ffma2_rn(make_float2(av[a].z, av[a].w), make_float2(bv[b].z, bv[b].w), s[a][b]);
+            s[a][b] = __ffma2_rn(a01, b01[b], s[a][b]);
+            s[a][b] = __ffma2_rn(a23, b23[b], s[a][b]);
           }
+        }
       }
       __syncwarp();  // with NH == 1 the Gram overwrites the rows every lane has finished reading
 #pragma unroll
