@@ -414,7 +414,7 @@ def run_ours(args, w):
         e2e["elapsed_ms"] = max_over_ranks(e2e["elapsed_ms"], world, dev)
         e2e = {"value": aggregate(evictions_per_step * e2e["steps"], e2e["elapsed_ms"] / 1e3, world),
                "unit": "evictions/s", "h2d_bytes_per_step": e2e["h2d"],
-               "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"]}
+               "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"], "h2d_warmup": e2e["h2d_warmup"]}
 
     bkv.bkv_destroy(h)
 
@@ -562,14 +562,15 @@ def e2e_plan(period_bytes: int, warmup: int, steps: int, host_cap_bytes: int):
 
 
 def run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, stream, state, dev, cs,
-            host_cap_bytes=48 << 30):
+            host_cap_bytes=48 << 30, nbuf=2, copy_events=None, warm_link=True):
     """Same step through the C ABI, with each step's inputs coming from pinned
     host memory (the period's queries and the new K/V rows) and the keep sets
     going back to the host, all inside the timed region. The copies run on a
-    second stream, double-buffered, so that step k + 1's inputs travel while
-    step k's eviction runs: inputs land in device staging buffers, and the new
-    K/V rows move into the cache (a device copy) once the eviction that reads
-    those slots is done.
+    second stream into nbuf staging buffers (default two), so that the next
+    steps' inputs travel while step k's eviction runs: inputs land in device
+    staging buffers, and the new K/V rows move into the cache (a device copy)
+    once the eviction that reads those slots is done. copy_events, when a
+    list, receives per step the (start, end) timing events of its input copy.
 
     Every step gets a period of fresh queries and fresh keys and values from
     the stream (a repeated period would hand FPS exact duplicates and the
@@ -597,27 +598,34 @@ def run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, stream, state, dev,
     del tmp
     write_tail = TailWriter(w)
     xs = torch.cuda.Stream(dev)
-    qstage = [torch.empty(q_host.shape[1:], dtype=q_host.dtype, device=dev) for _ in range(2)]
-    tstage = [torch.empty(tail_host.shape[1:], dtype=tail_host.dtype, device=dev) for _ in range(2)]
-    kept_dev = [kept, torch.empty_like(kept)]
-    kept_host = [torch.empty(kept.shape, dtype=kept.dtype).pin_memory() for _ in range(2)]
-    ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("staged", "used", "evicted", "read")}
+    qstage = [torch.empty(q_host.shape[1:], dtype=q_host.dtype, device=dev) for _ in range(nbuf)]
+    link = warm_h2d(q_host[0], qstage[0], xs) if warm_link else None
+    tstage = [torch.empty(tail_host.shape[1:], dtype=tail_host.dtype, device=dev) for _ in range(nbuf)]
+    kept_dev = [kept] + [torch.empty_like(kept) for _ in range(nbuf - 1)]
+    kept_host = [torch.empty(kept.shape, dtype=kept.dtype).pin_memory() for _ in range(nbuf)]
+    ev = {name: [torch.cuda.Event() for _ in range(nbuf)] for name in ("staged", "used", "evicted", "read")}
 
     def stage(k):
-        """Copy stream: step k's queries and new K/V rows into staging buffer k % 2."""
-        b = k % 2
+        """Copy stream: step k's queries and new K/V rows into staging buffer k % nbuf."""
+        b = k % nbuf
         with torch.cuda.stream(xs):
-            if k >= 2:
-                xs.wait_event(ev["used"][b])  # step k - 2 is done with this buffer
+            if k >= nbuf:
+                xs.wait_event(ev["used"][b])  # step k - nbuf is done with this buffer
+            if copy_events is not None:
+                ce = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ce[0].record(xs)
             qstage[b].copy_(q_host[k], non_blocking=True)
             tstage[b].copy_(tail_host[k], non_blocking=True)
+            if copy_events is not None:
+                ce[1].record(xs)
+                copy_events.append(ce)
             ev["staged"][b].record(xs)
 
     def step(k):
-        b = k % 2
+        b = k % nbuf
         t = state["t"]
-        if k >= 2:
-            cs.wait_event(ev["read"][b])  # step k - 2's keep sets have reached the host
+        if k >= nbuf:
+            cs.wait_event(ev["read"][b])  # step k - nbuf's keep sets have reached the host
         bkv.bkv_evict_ptrs(h, kptr, vptr, w.max_cache, t, kept_dev[b].data_ptr())
         ev["evicted"][b].record(cs)
         with torch.cuda.stream(xs):
@@ -632,25 +640,51 @@ def run_e2e(args, w, bkv, h, K_all, V_all, kept, kptr, vptr, stream, state, dev,
         ev["used"][b].record(cs)
         state["t"] = t + w.period
 
-    stage(0)
-    stage(1)
+    for k in range(min(nbuf, total)):
+        stage(k)
     for k in range(warm):
         step(k)
-        if k + 2 < total:
-            stage(k + 2)
+        if k + nbuf < total:
+            stage(k + nbuf)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(cs)
     for k in range(warm, total):
         step(k)
-        if k + 2 < total:
-            stage(k + 2)
-    cs.wait_event(ev["read"][(total - 1) % 2])  # the last keep sets are on the host
+        if k + nbuf < total:
+            stage(k + nbuf)
+    cs.wait_event(ev["read"][(total - 1) % nbuf])  # the last keep sets are on the host
     e1.record(cs)
     torch.cuda.synchronize(dev)
     bkv.bkv_sync(h)
     return {"elapsed_ms": e0.elapsed_time(e1), "steps": steps,
-            "h2d": qstage[0].numel() * 2 + tstage[0].numel() * 2, "d2h": kept_host[0].numel() * 4}
+            "h2d": qstage[0].numel() * 2 + tstage[0].numel() * 2, "d2h": kept_host[0].numel() * 4,
+            "h2d_warmup": link}
+
+
+def warm_h2d(src, dst, xs, min_gbs=100.0, need=3, max_copies=40):
+    """Untimed warm-up of the host-to-device path before the e2e region.
+    Without it, on the GB300 machines, the first six to nine staged copies of a
+    run (about half a second) took 45-135 ms for 1.36 GB (10-30 GB/s) before
+    settling at 6-10 ms, whatever buffer was copied, and the e2e rate ranged
+    from 165K to 260K evictions/s; with it (3-4 copies of one step's queries
+    at ~210 GB/s) four runs gave 263K-272K. Repeats the copy until `need`
+    copies in a row reach min_gbs (at most max_copies); returns the copies
+    made and the last rate."""
+    import torch
+    nbytes = src.numel() * src.element_size()
+    run, gbs, n = 0, 0.0, 0
+    while n < max_copies and run < need:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(xs):
+            a.record(xs)
+            dst.copy_(src, non_blocking=True)
+            b.record(xs)
+        b.synchronize()
+        gbs = nbytes / (a.elapsed_time(b) / 1e3) / 1e9
+        run = run + 1 if gbs >= min_gbs else 0
+        n += 1
+    return {"copies": n, "last_gbs": gbs}
 
 
 def kernel_source_digest(kernel: str):
