@@ -4,7 +4,10 @@ side by side and compares every eviction.
 Agreement rules (per unit and eviction):
   * state before the eviction: every query head's beacons and recent ring equal
     the oracle's, byte for byte (covers every FPS that ran during appends);
-  * scores: |s_gpu - s_orc| <= 1e-6 + 2e-3 * |s_orc| for every slot j < L;
+  * scores: |s_gpu - s_orc| <= 1e-6 + 2e-3 * |s_orc| for every slot j < L
+    (with keep_scores=False the handle keeps no scores, as in the bench, and
+    only the keep set, the compaction and the FPS state are compared, the
+    keep set still against the oracle's scores);
   * keep set: exactly `budget` ascending slots, containing the prefix and the
     recent window, and identical to the oracle's on every candidate whose
     oracle score lies farther than 1e-6 + 2e-3 * s_k from s_k, the k_sel-th
@@ -76,7 +79,7 @@ class GpuUnitResult:
     """One unit's library outputs at one eviction, copied to the host."""
     nb: int                # beacons per query head before the eviction
     state: list            # per query head: uint16 [fps_cap + n_rq][d] before the eviction
-    scores: np.ndarray     # float32 [L]
+    scores: np.ndarray     # float32 [L], or None when the handle keeps no scores
     layout: list           # kept slots (ascending), or the order-free layout
     K: np.ndarray          # uint16 [budget][d] after the compaction
     V: np.ndarray
@@ -96,15 +99,16 @@ def check_unit(uo, unit, t, L, w, res: GpuUnitResult, order_free, rep, fail) -> 
             fail(f"t={t} unit {unit} head {hg}: beacon/recent state differs")
             return False
     s_orc, _ = uo.scores(t)
-    s_gpu = np.asarray(res.scores, dtype=np.float64)
-    err = np.abs(s_gpu - s_orc)
-    tol = SCORE_ATOL + SCORE_RTOL * np.abs(s_orc)
-    rel = float(np.max(err / np.maximum(np.abs(s_orc), 1e-30)))
-    rep.max_score_rel = max(rep.max_score_rel, rel)
-    if np.any(err > tol):
-        j = int(np.argmax(err - tol))
-        fail(f"t={t} unit {unit}: score[{j}] gpu {s_gpu[j]:.9g} orc {s_orc[j]:.9g}")
-        return False
+    if res.scores is not None:
+        s_gpu = np.asarray(res.scores, dtype=np.float64)
+        err = np.abs(s_gpu - s_orc)
+        tol = SCORE_ATOL + SCORE_RTOL * np.abs(s_orc)
+        rel = float(np.max(err / np.maximum(np.abs(s_orc), 1e-30)))
+        rep.max_score_rel = max(rep.max_score_rel, rel)
+        if np.any(err > tol):
+            j = int(np.argmax(err - tol))
+            fail(f"t={t} unit {unit}: score[{j}] gpu {s_gpu[j]:.9g} orc {s_orc[j]:.9g}")
+            return False
     orc_kept = select_keep(s_orc, L, w.prefix, w.recent, w.budget)
     g_layout = [int(x) for x in res.layout]
     g_kept = sorted(g_layout) if order_free else g_layout
@@ -134,7 +138,7 @@ def check_unit(uo, unit, t, L, w, res: GpuUnitResult, order_free, rep, fail) -> 
 def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "cpu",
                  steps: int | None = None, max_failures: int = 20,
                  query_hook=None, order_free: bool = False, pool: str = "max",
-                 coverage_n: int = 0, prefill: int = 0) -> LockstepReport:
+                 coverage_n: int = 0, prefill: int = 0, keep_scores: bool = True) -> LockstepReport:
     from kv_cache_eviction_head_gb300 import bkv
 
     dev = torch.device("cuda")
@@ -149,7 +153,7 @@ def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "c
                           period=w.period, prefix=w.prefix, recent=w.recent, fps_cap=w.fps_cap,
                           fps_keep=w.fps_keep, layers=w.layers, batch=w.batch,
                           max_cache=w.max_cache, rope_theta=w.theta,
-                          flags=bkv.BKV_FLAG_KEEP_SCORES
+                          flags=(bkv.BKV_FLAG_KEEP_SCORES if keep_scores else 0)
                           | (bkv.BKV_FLAG_ORDER_FREE if order_free else 0)
                           | (bkv.BKV_FLAG_MEAN_POOL if pool == "mean" else 0))
     ws = torch.empty(bkv.bkv_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
@@ -205,12 +209,13 @@ def run_lockstep(w: Workload, seed: int, sample_units=None, gen_device: str = "c
         bkv.bkv_evict(h, K, V, cache_len, t, kept)
         bkv.bkv_sync(h)
         rep.evictions += 1
-        scores = bkv.bkv_get_scores(h)
+        scores = bkv.bkv_get_scores(h) if keep_scores else None
         traces = bkv.bkv_get_fps_trace(h)
         kept_h = kept.cpu().numpy()
         for (l, b, kh) in sorted(live):
             u = (l, b, kh)
-            res = GpuUnitResult(nb=nb_gpu, state=states[u], scores=scores[l, b, kh, :cache_len],
+            res = GpuUnitResult(nb=nb_gpu, state=states[u],
+                                scores=scores[l, b, kh, :cache_len] if keep_scores else None,
                                 layout=kept_h[l, b, kh].tolist(),
                                 K=to_bits(K[l][b, kh, :w.budget]), V=to_bits(V[l][b, kh, :w.budget]),
                                 traces=[traces[l, b, kh * G + hg].tolist() for hg in range(G)])
@@ -338,7 +343,7 @@ def _unit_worker(w: Workload, seed: int, units: list, order_free: bool, pool: st
 
 def run_lockstep_parallel(w: Workload, seed: int, sample_units=None, steps: int | None = None,
                           workers: int | None = None, order_free: bool = False,
-                          pool: str = "max") -> LockstepReport:
+                          pool: str = "max", keep_scores: bool = True) -> LockstepReport:
     """run_lockstep's agreement rules on many units at once: the library runs
     the stream (generated on the CPU) in this process, and the oracles of the
     sampled units run in `workers` spawned child processes that regenerate the
@@ -392,7 +397,7 @@ def run_lockstep_parallel(w: Workload, seed: int, sample_units=None, steps: int 
                           period=w.period, prefix=w.prefix, recent=w.recent, fps_cap=w.fps_cap,
                           fps_keep=w.fps_keep, layers=w.layers, batch=w.batch,
                           max_cache=w.max_cache, rope_theta=w.theta,
-                          flags=bkv.BKV_FLAG_KEEP_SCORES
+                          flags=(bkv.BKV_FLAG_KEEP_SCORES if keep_scores else 0)
                           | (bkv.BKV_FLAG_ORDER_FREE if order_free else 0)
                           | (bkv.BKV_FLAG_MEAN_POOL if pool == "mean" else 0))
     ws = torch.empty(bkv.bkv_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
@@ -418,7 +423,7 @@ def run_lockstep_parallel(w: Workload, seed: int, sample_units=None, steps: int 
             bkv.bkv_evict(h, K, V, cache_len, t, kept)
             bkv.bkv_sync(h)
             main.evictions += 1
-            scores = bkv.bkv_get_scores(h)
+            scores = bkv.bkv_get_scores(h) if keep_scores else None
             traces = bkv.bkv_get_fps_trace(h)
             kept_h = kept.cpu().numpy()
             kv_h = {l: (to_bits(K[l][:, :, :w.budget]), to_bits(V[l][:, :, :w.budget])) for l in layers}
@@ -426,7 +431,7 @@ def run_lockstep_parallel(w: Workload, seed: int, sample_units=None, steps: int 
             for u in sample_units:
                 l, b, kh = u
                 msgs[owner[u]][u] = GpuUnitResult(
-                    nb=nb, state=states[u], scores=scores[l, b, kh, :cache_len].copy(),
+                    nb=nb, state=states[u], scores=scores[l, b, kh, :cache_len].copy() if keep_scores else None,
                     layout=kept_h[l, b, kh].tolist(), K=kv_h[l][0][b, kh].copy(), V=kv_h[l][1][b, kh].copy(),
                     traces=[traces[l, b, kh * G + hg].tolist() for hg in range(G)])
             for i, m in enumerate(msgs):

@@ -162,6 +162,18 @@ def test_qwen3_4b_b192_full_size_sampled_units():
     assert rep.units_checked == len(units) * rep.evictions
 
 
+def test_qwen3_4b_b192_full_size_without_kept_scores():
+    """The bench's own handle configuration (no per-key scores kept) at full
+    size: keep sets judged against the oracle's scores, compaction and FPS
+    state byte-exact, three evictions on sampled units."""
+    w = WORKLOADS["qwen3_4b_b192"]
+    units = [(1, 5, 4), (30, 190, 2), (12, 77, 7), (35, 0, 0)]
+    rep = run_lockstep(w, seed=0xBEADA, sample_units=units, gen_device="cuda",
+                       steps=w.max_cache + 2 * w.period, keep_scores=False)
+    assert_clean(rep, min_evictions=3)
+    assert rep.units_checked == len(units) * rep.evictions
+
+
 def test_qwen3_14b_b64_full_size_sampled_units():
     """Qwen3-14B head shape (GQA 5, 160 observation rows, budget 1024) at
     batch 64: full-size cache, three evictions, sampled units."""
