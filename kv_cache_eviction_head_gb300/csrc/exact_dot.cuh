@@ -123,5 +123,29 @@ __device__ double exact_dot(const uint4* xi, const uint4* xj, int emin_i, int em
   return acc == 0 ? 0.0 : __dmul_rn(__ll2double_rn(acc), pow2(emin_i + emin_j));
 }
 
+// exact_dot evaluated by a whole warp on one pair of rows (every lane passes
+// the same arguments and gets the same result): lane l takes elements
+// l, l + 32, l + 64, l + 96, and the exact 64-bit integer partial sums are
+// added exactly across the warp before the one rounding, so the value is
+// exact_dot's, bit for bit. Wide pairs take exact_dot_wide on every lane.
+__device__ double exact_dot_warp(const uint4* xi, const uint4* xj, int emin_i, int emin_j, bool wide) {
+  if (wide) return exact_dot_wide(xi, xj);
+  const int lane = threadIdx.x & 31;
+  long long acc = 0;
+#pragma unroll
+  for (int q = 0; q < kD / 32; ++q) {
+    const int k = lane + 32 * q;
+    int sa, ea, na, fa, sb, eb, nbv, fb;
+    decode_bf16(elem(xi, k), sa, ea, na, fa);
+    decode_bf16(elem(xj, k), sb, eb, nbv, fb);
+    if (sa == 0 || sb == 0 || fa || fb) continue;
+    const long long p = (long long)(sa << (ea - emin_i)) * (long long)(sb << (eb - emin_j));
+    acc += (na ^ nbv) ? -p : p;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  return acc == 0 ? 0.0 : __dmul_rn(__ll2double_rn(acc), pow2(emin_i + emin_j));
+}
+
 }  // namespace
 }  // namespace bkv

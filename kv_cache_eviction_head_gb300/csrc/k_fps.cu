@@ -18,15 +18,28 @@
 //     shared memory as bf16 (exact, apart from components more than 126
 //     binades below the largest, which round to the bf16 subnormal grid with
 //     an error below 2^-134);
-//   * the float32 Gram entry is two interleaved sums (even and odd k) of 64
-//     bf16 products each (exact, or below 2^-149 off where a product
-//     underflows), added once, so its error is at most
+//   * up to 32 candidates (one 32-row block per head): the Gram comes from the
+//     tensor cores. A CTA stacks its four heads' rows into one 128 x 128 bf16
+//     operand, one thread issues G = Y Y^T (tcgen05.mma, fp32 accumulators in
+//     128 TMEM columns) and each warp reads its head's 32 x 32 diagonal block,
+//     one Gram row per lane. The products are exact; the accumulation order
+//     and rounding are the hardware's, so the bound used assumes only fp32
+//     precision at each of the 127 additions with any rounding direction:
+//     |G32 - G| <= 127 * 2^-23 * sum_k |y_ik y_jk| <= 1.52e-5 ||y_i|| ||y_j||
+//     (products of bf16 subnormals, if flushed, add below 2^-100 relative). A
+//     probe of 128 x 128 x 128 Grams (normal, near-duplicate, wide-exponent,
+//     cancelling and two-scale rows) measured at most 10.8 * 2^-24 of
+//     sum_k |y_ik y_jk|, a twentieth of the bound;
+//   * up to 64 candidates: the float32 Gram entry is two interleaved sums
+//     (even and odd k) of 64 bf16 products each (exact, or below 2^-149 off
+//     where a product underflows), added once, so its error is at most
 //     gamma_64 * ||y_i|| ||y_j|| (3.8e-6 relative) plus < 2^-123 from the
 //     subnormal roundings, against ||y_i|| >= 2^-7 for every nonzero row;
-//   * c_ij = (G32_ij * r_i) * r_j with r_i = rsqrtf(G32_ii) (2 ulp) is then
-//     within 8.5e-6 of the float64 cosine; the filters use kCosErr = 2e-5;
+//   * c_ij = (G32_ij * r_i) * r_j with r_i = rsqrtf(G32_ii) (2 ulp, on a
+//     diagonal within 1.52e-5 relative) is then within 3.2e-5 of the float64
+//     cosine (8.5e-6 for the float32 Gram); the filters use kCosErr = 4e-5;
 //   * the mean a_i in float32 (any summation order, N <= 64) is within
-//     8.5e-6 + 63 * 2^-24 of the float64 mean; the filters use kMeanErr;
+//     3.2e-5 + 63 * 2^-24 of the float64 mean; the filters use kMeanErr;
 //   * a decision (argmin of the mean cosine, argmin of the running max) is
 //     final when the float32 minimum beats every other candidate by more than
 //     twice its error bound - then the float64 values order the same way;
@@ -43,26 +56,29 @@
 
 #include "bkv_internal.cuh"
 #include "exact_dot.cuh"
+#include "score_common.cuh"  // mbarrier, TMEM and tcgen05 wrappers
 
 namespace bkv {
 
 namespace {
 
-constexpr int kHeadsPerCta = 2;       // one warp per head
+// one warp per head; up to 32 candidates four heads share one tensor-core Gram
+template <int NH>
+constexpr int kHeadsPerCta = NH == 1 ? 4 : 2;
 constexpr int kMaxCand = 64;          // beacons (< fps_cap <= 32) + recents (<= 32)
 constexpr int kYStride = kD + 8;      // bf16 row stride (272 bytes): 16-byte aligned rows, and LDS.64 of 8 consecutive rows hit distinct banks
-constexpr float kCosErr = 2e-5f;      // |c32 - cos64| bound used by the filters
-constexpr float kMeanErr = 2.5e-5f;   // |a32 - a64| bound used by the filters
-constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr float kCosErr = 4e-5f;      // |c32 - cos64| bound used by the filters
+constexpr float kMeanErr = 4.5e-5f;   // |a32 - a64| bound used by the filters
+constexpr int kGramCols = 128;        // TMEM columns of the tensor-core Gram (4 heads x 32)
+constexpr float kInfF = __builtin_huge_valf();
 
 // Per-warp shared memory for NT = 32 * NH candidate slots.
 template <int NH>
 struct WarpSmem {
   static constexpr int NT = 32 * NH;
-  static constexpr size_t kY = (((size_t)NT * kYStride * 2 + 15) / 16) * 16;
-  // NH == 1: the cosine matrix reuses the rows' space once the Gram is in registers
-  static constexpr size_t kC = NH == 1 ? 0 : (((size_t)NT * (NT + 1) * 4 + 15) / 16) * 16;
-  static_assert(NH != 1 || (size_t)NT * (NT + 1) * 4 <= kY, "the cosine matrix fits in the rows' space");
+  // NH == 1: the rows live in the CTA's tensor-core operand instead
+  static constexpr size_t kY = NH == 1 ? 0 : (((size_t)NT * kYStride * 2 + 15) / 16) * 16;
+  static constexpr size_t kC = (((size_t)NT * (NT + 1) * 4 + 15) / 16) * 16;
   static constexpr size_t kMisc = (size_t)NT * 8 * 2 + (size_t)NT * 4 * 5 + 64 * 4;
   static constexpr size_t kBytes = ((kY + kC + kMisc) + 15) / 16 * 16;
 
@@ -80,7 +96,7 @@ struct WarpSmem {
 
   __device__ WarpSmem(unsigned char* base) {
     y = reinterpret_cast<__nv_bfloat16*>(base);
-    c = NH == 1 ? reinterpret_cast<float*>(base) : reinterpret_cast<float*>(base + kY);
+    c = reinterpret_cast<float*>(base + kY);
     unsigned char* m = base + kY + kC;
     diag = reinterpret_cast<double*>(m);
     v64 = diag + NT;
@@ -149,16 +165,47 @@ __device__ __forceinline__ int filtered_argmin(int* cand, float v0, float v1, bo
   return best;
 }
 
+// Dynamic shared memory of one CTA (NH == 1: the 1024-aligned 128 x 128 bf16
+// operand of the Gram, then the warps' blocks).
 template <int NH>
-__global__ void __launch_bounds__(32 * kHeadsPerCta, 8) fps_kernel(FpsParams P) {
+constexpr size_t fps_cta_smem() {
+  return (NH == 1 ? 1024 + (size_t)kTileBytes : 0) + WarpSmem<NH>::kBytes * kHeadsPerCta<NH>;
+}
+
+template <int NH>
+__global__ void __launch_bounds__(32 * kHeadsPerCta<NH>, NH == 1 ? 4 : 8) fps_kernel(FpsParams P) {
   using W = WarpSmem<NH>;
   constexpr int NT = W::NT;
   extern __shared__ __align__(16) unsigned char fps_smem[];
+  __shared__ uint64_t gram_bar[4];  // NH == 1: one per warp, its Gram product is done
+  __shared__ uint32_t gram_tmem;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t head = (int64_t)blockIdx.x * kHeadsPerCta + warp;
-  if (head >= P.heads_total) return;
   const int nb = P.nb, n = P.nb + P.nr, m = P.m;
-  W sm(fps_smem + (size_t)warp * W::kBytes);
+  unsigned char* opnd = fps_smem;  // NH == 1: the Gram's operand, rows 32 * warp + r
+  unsigned char* wbase = fps_smem;
+  if constexpr (NH == 1) {
+    opnd = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(fps_smem) + 1023) & ~(uintptr_t)1023);
+    wbase = opnd + kTileBytes;
+  }
+  W sm(wbase + (size_t)warp * W::kBytes);
+  // NH == 1 with sampling: persistent CTAs of four warps; each warp takes a
+  // head at a time and multiplies the CTA's 128-row operand by its own 32
+  // rows into its own 32 TMEM columns, so the warps never wait on each other
+  const bool tc = NH == 1 && n > m;  // the same for the whole launch
+  if (tc) {
+    if (warp == 0) tmem_alloc(&gram_tmem, kGramCols);
+    if (threadIdx.x == 0) {
+      for (int w = 0; w < 4; ++w) mbar_init(&gram_bar[w], 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  const uint32_t tmem = tc ? gram_tmem : 0u;
+  uint32_t gph = 0u;  // parity of this warp's Gram barrier
+  const int64_t stride = (int64_t)gridDim.x * kHeadsPerCta<NH>;
+  for (int64_t head = (int64_t)blockIdx.x * kHeadsPerCta<NH> + warp; head < P.heads_total; head += stride) {
   uint4* bq = P.bq + head * P.fps_cap * 16;
   const uint4* rq = P.rq + head * P.n_rq * 16;
   // candidates: beacons (oldest first), then recents (oldest first)
@@ -202,18 +249,53 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta, 8) fps_kernel(FpsParams P) 
           o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
         }
-        *reinterpret_cast<uint4*>(sm.y + r * kYStride + part * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+        if constexpr (NH == 1)  // SWIZZLE_128B K-major: 64-column slabs of 128-byte rows
+          *reinterpret_cast<uint4*>(opnd + (part >> 3) * kSlabBytes + (32 * warp + r) * 128 +
+                                    (((part & 7) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        else
+          *reinterpret_cast<uint4*>(sm.y + r * kYStride + part * 8) = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
     if (__any_sync(kFull, bad) && lane == 0) latch(P.status, BKV_ERR_NONFINITE);
     __syncwarp();
 
-    // ---- float32 Gram, 32 x 32 tiles; lane (I, J) = (lane & 7, lane >> 3)
+    // ---- tensor-core Gram (NH == 1): this warp's 32 rows against the CTA's
+    // 128-row operand, D = Y_cta Y_w^T into columns 32 w; the rows 32 w.. of D
+    // are this head's Gram (the other rows, from the other warps' heads, are
+    // not read)
+    float gr[32];  // NH == 1: row `lane` of this head's Gram
+    if constexpr (NH == 1) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();  // this warp's reads of its columns (previous head) are complete
+      __syncwarp();
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t a0 = smem_u32(opnd), b0 = a0 + (uint32_t)(32 * warp * 128);
+        const uint32_t id = idesc_bf16(128, 32);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * kSlabBytes + (uint32_t)(kk & 3) * 32;
+          umma_bf16(tmem + (uint32_t)(32 * warp), sw128_desc(a0 + off), sw128_desc(b0 + off), id, kk ? 1u : 0u);
+        }
+        umma_commit(&gram_bar[warp]);
+      }
+      // bounded wait: a product that never completes latches BKV_ERR_TIMEOUT
+      bool done = mbar_test(&gram_bar[warp], gph);
+      const long long t0 = clock64();
+      while (!done && clock64() - t0 < kWaitCycles) done = mbar_test(&gram_bar[warp], gph);
+      if (!__all_sync(kFull, done) && lane == 0) latch(P.status, BKV_ERR_TIMEOUT);
+      gph ^= 1u;
+      tc_fence_after();
+      tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * warp), gr);
+      tmem_wait_ld();
+    }
+
+    // ---- float32 Gram (NH == 2), 32 x 32 tiles; lane (I, J) = (lane & 7, lane >> 3)
     // owns rows I + 8a (a < 4) and columns J + 4b (b < 8) of a tile, so each
     // LDS.128 touches 8 (or 4) consecutive rows: distinct banks
     const int I = lane & 7, J = lane >> 3;
 #pragma unroll 1
-    for (int tile = 0; tile < (NH == 1 ? 1 : 3); ++tile) {
+    for (int tile = 0; tile < (NH == 1 ? 0 : 3); ++tile) {
       const int ti = tile == 2 ? 1 : 0, tj = tile == 0 ? 0 : 1;
       const __nv_bfloat16* ya = sm.y + (ti * 32 + I) * kYStride;
       const __nv_bfloat16* yb = sm.y + (tj * 32 + J) * kYStride;
@@ -248,7 +330,6 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta, 8) fps_kernel(FpsParams P) 
           }
         }
       }
-      __syncwarp();  // with NH == 1 the Gram overwrites the rows every lane has finished reading
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -262,12 +343,29 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta, 8) fps_kernel(FpsParams P) 
     __syncwarp();
 
     // ---- cosines, row i by lane i (and i + 32), with the row sums for the means
+    float a[NH];
+    if constexpr (NH == 1) {
+      float gd = 0.f;  // the diagonal entry of this lane's row
+#pragma unroll
+      for (int q = 0; q < 32; ++q) gd = q == lane ? gr[q] : gd;
+      const float ri = gd > 0.f ? rsqrtf(gd) : 0.f;
+      float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float v = __fmul_rn(__fmul_rn(gr[j], ri), __shfl_sync(kFull, ri, j));
+        sm.C(lane, j) = v;
+        if (j < n) {
+          if (j & 1) acc1 = __fadd_rn(acc1, v);
+          else acc0 = __fadd_rn(acc0, v);
+        }
+      }
+      a[0] = __fdiv_rn(__fadd_rn(acc0, acc1), (float)n);
+    } else {
     for (int i = lane; i < NT; i += 32) {
       const float g = sm.C(i, i);
       sm.inv[i] = g > 0.f ? rsqrtf(g) : 0.f;
     }
     __syncwarp();
-    float a[NH];
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
       const int i = lane + 32 * h;
@@ -283,38 +381,53 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta, 8) fps_kernel(FpsParams P) 
       }
       a[h] = __fdiv_rn(__fadd_rn(acc0, acc1), (float)n);
     }
+    }
     __syncwarp();
 
-    // ---- exact path, prepared on the first close call of this head
-    bool meta_ok = false;
-    auto meta = [&]() {
-      if (meta_ok) return;
-      for (int r = lane; r < n; r += 32) {
-        const uint4* x = row(r);
-        int emin = INT_MAX, emax = INT_MIN;
-        for (int k = 0; k < kD; ++k) {
-          int sig, e, neg, nf;
-          decode_bf16(elem(x, k), sig, e, neg, nf);
-          if (sig != 0 && !nf) {
-            emin = min(emin, e);
-            emax = max(emax, e);
-          }
+    // ---- exact path: per-row data (exponent range, exact G_ii) made when a
+    // close call first needs the row; bit r of `ready` marks row r
+    unsigned long long ready = 0ull;  // the same on every lane
+    auto ensure = [&](int r) {
+      if ((ready >> r) & 1ull) return;
+      const uint4* x = row(r);
+      int emin = INT_MAX, emax = INT_MIN;
+#pragma unroll
+      for (int q = 0; q < kD / 32; ++q) {
+        int sig, e, neg, nf;
+        decode_bf16(elem(x, lane + 32 * q), sig, e, neg, nf);
+        if (sig != 0 && !nf) {
+          emin = min(emin, e);
+          emax = max(emax, e);
         }
-        if (emin == INT_MAX) emin = emax = 0;
-        const bool wide = emax - emin > 20;
+      }
+      emin = __reduce_min_sync(kFull, emin);
+      emax = __reduce_max_sync(kFull, emax);
+      if (emin == INT_MAX) emin = emax = 0;
+      const bool wide = emax - emin > 20;
+      const double d = exact_dot_warp(x, x, emin, emin, wide);
+      if (lane == 0) {
         sm.emin[r] = emin;
         sm.emax[r] = emax;
         sm.wide[r] = wide;
-        sm.diag[r] = exact_dot(x, x, emin, emin, wide);
+        sm.diag[r] = d;
       }
       __syncwarp();
-      meta_ok = true;
+      ready |= 1ull << r;
     };
-    // the float64 cosine of the reference arithmetic
+    // the float64 cosine of the reference arithmetic; cos64 by one lane (rows
+    // ready), cos64w by the whole warp
     auto cos64 = [&](int i, int j) -> double {
       const double gii = sm.diag[i], gjj = sm.diag[j];
       if (gii == 0.0 || gjj == 0.0) return 0.0;
       const double g = exact_dot(row(i), row(j), sm.emin[i], sm.emin[j], sm.wide[i] | sm.wide[j]);
+      return __ddiv_rn(g, __dsqrt_rn(__dmul_rn(gii, gjj)));
+    };
+    auto cos64w = [&](int i, int j) -> double {
+      ensure(i);
+      ensure(j);
+      const double gii = sm.diag[i], gjj = sm.diag[j];
+      if (gii == 0.0 || gjj == 0.0) return 0.0;
+      const double g = exact_dot_warp(row(i), row(j), sm.emin[i], sm.emin[j], sm.wide[i] | sm.wide[j]);
       return __ddiv_rn(g, __dsqrt_rn(__dmul_rn(gii, gjj)));
     };
 
@@ -324,7 +437,7 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta, 8) fps_kernel(FpsParams P) 
     // exact mean cosine of candidate i: lanes evaluate cos64(i, j) for their j,
     // every lane sums them left to right
     auto mean64 = [&](int i) -> double {
-      meta();
+      for (int r = 0; r < n; ++r) ensure(r);
       for (int j = lane; j < n; j += 32) sm.v64[j] = cos64(i, j);
       __syncwarp();
       double acc = 0.0;
@@ -337,15 +450,27 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta, 8) fps_kernel(FpsParams P) 
     bool ch0 = i0 == p0, ch1 = i1 == p0;
     float S0 = live0 ? sm.C(i0, p0) : 0.f, S1 = live1 ? sm.C(i1, p0) : 0.f;
     for (int k = 1; k < m; ++k) {
-      // exact running maximum of candidate j over the picks so far
+      // exact running maximum of candidate j over the picks so far: only the
+      // picks whose float32 cosine lies within twice the bound of the float32
+      // maximum can hold it (every other one is below that pick's float64 value)
       auto smax64 = [&](int j) -> double {
-        meta();
+        float c32 = -kInfF;
+        for (int q = lane; q < k; q += 32) c32 = fmaxf(c32, sm.C(j, sm.picks[q]));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) c32 = fmaxf(c32, __shfl_xor_sync(kFull, c32, off));
+        const float lim = c32 - 2.0f * kCosErr;
         double v = -__longlong_as_double(0x7ff0000000000000LL);
-        for (int q = lane; q < k; q += 32) {
-          const double c = cos64(j, sm.picks[q]);
-          v = c > v ? c : v;
+        for (int q0 = 0; q0 < k; q0 += 32) {
+          const int q = q0 + lane;
+          unsigned near = __ballot_sync(kFull, q < k && !(sm.C(j, sm.picks[q]) < lim));
+          while (near) {
+            const int qq = q0 + __ffs(near) - 1;
+            near &= near - 1;
+            const double c = cos64w(j, sm.picks[qq]);
+            v = c > v ? c : v;
+          }
         }
-        return warp_max64(v);
+        return v;
       };
       __syncwarp();
       const int r = filtered_argmin(sm.cand, S0, S1, live0 && !ch0, live1 && !ch1, kCosErr, smax64);
@@ -369,27 +494,37 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta, 8) fps_kernel(FpsParams P) 
   }
   __syncwarp();
 
-  // ---- kept rows back into the beacon buffer; every source row is read
-  // before any is overwritten (m <= 31 rows of 16 uint4: <= 16 per lane)
-  const int kept = n < m ? n : m;
-  uint4 buf[16];
+  {
+    // ---- kept rows back into the beacon buffer; every source row is read
+    // before any is overwritten (m <= 31 rows of 16 uint4: <= 16 per lane)
+    const int kept = n < m ? n : m;
+    uint4 buf[16];
 #pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    const int idx = lane + 32 * q;
-    if (idx < kept * 16 && BKV_IN_RANGE(sm.keep_src[idx >> 4] >= 0 && sm.keep_src[idx >> 4] < n, P.status))
-      buf[q] = row(sm.keep_src[idx >> 4])[idx & 15];
+    for (int q = 0; q < 16; ++q) {
+      const int idx = lane + 32 * q;
+      if (idx < kept * 16 && BKV_IN_RANGE(sm.keep_src[idx >> 4] >= 0 && sm.keep_src[idx >> 4] < n, P.status))
+        buf[q] = row(sm.keep_src[idx >> 4])[idx & 15];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int idx = lane + 32 * q;
+      if (idx < kept * 16) bq[idx] = buf[q];
+    }
   }
-  __syncwarp();
-#pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    const int idx = lane + 32 * q;
-    if (idx < kept * 16) bq[idx] = buf[q];
+  __syncwarp();  // the next head reuses this warp's rows and cosines
+  }
+  if (tc) {  // every warp is done reading the Gram: free its columns
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(gram_tmem, kGramCols);
   }
 }
 
 template <int NH>
 cudaError_t launch_nh(const FpsParams& p, cudaStream_t s) {
-  const size_t smem = WarpSmem<NH>::kBytes * kHeadsPerCta;
+  const size_t smem = fps_cta_smem<NH>();
   static std::atomic<unsigned long long> configured{0};  // one bit per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -400,8 +535,14 @@ cudaError_t launch_nh(const FpsParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  const int64_t blocks = (p.heads_total + kHeadsPerCta - 1) / kHeadsPerCta;
-  fps_kernel<NH><<<(unsigned)blocks, 32 * kHeadsPerCta, smem, s>>>(p);
+  int64_t blocks = (p.heads_total + kHeadsPerCta<NH> - 1) / kHeadsPerCta<NH>;
+  if (NH == 1 && p.nb + p.nr > p.m) {  // persistent: four CTAs per SM (their TMEM columns fill the SM's 512)
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    blocks = blocks < 4LL * sms ? blocks : 4LL * sms;
+  }
+  fps_kernel<NH><<<(unsigned)blocks, 32 * kHeadsPerCta<NH>, smem, s>>>(p);
   return cudaGetLastError();
 }
 
