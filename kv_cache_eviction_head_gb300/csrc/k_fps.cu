@@ -496,20 +496,28 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta<NH>, NH == 1 ? 4 : 8) fps_ke
 
   {
     // ---- kept rows back into the beacon buffer; every source row is read
-    // before any is overwritten (m <= 31 rows of 16 uint4: <= 16 per lane)
+    // before any is overwritten (m <= 31 rows of 16 uint4), through shared
+    // memory: NH == 1 this warp's operand rows (its product is done; the
+    // other warps' products only read them into rows of D nobody reads),
+    // NH == 2 the cosines
     const int kept = n < m ? n : m;
-    uint4 buf[16];
-#pragma unroll
+    auto stage = [&](int idx) -> uint4* {
+      if constexpr (NH == 1)
+        return reinterpret_cast<uint4*>(opnd + (idx >> 8) * kSlabBytes + 32 * warp * 128) + (idx & 255);
+      else
+        return reinterpret_cast<uint4*>(sm.c) + idx;
+    };
+#pragma unroll 4
     for (int q = 0; q < 16; ++q) {
       const int idx = lane + 32 * q;
       if (idx < kept * 16 && BKV_IN_RANGE(sm.keep_src[idx >> 4] >= 0 && sm.keep_src[idx >> 4] < n, P.status))
-        buf[q] = row(sm.keep_src[idx >> 4])[idx & 15];
+        *stage(idx) = row(sm.keep_src[idx >> 4])[idx & 15];
     }
     __syncwarp();
-#pragma unroll
+#pragma unroll 4
     for (int q = 0; q < 16; ++q) {
       const int idx = lane + 32 * q;
-      if (idx < kept * 16) bq[idx] = buf[q];
+      if (idx < kept * 16) bq[idx] = *stage(idx);
     }
   }
   __syncwarp();  // the next head reuses this warp's rows and cosines
