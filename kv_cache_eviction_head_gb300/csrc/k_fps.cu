@@ -19,10 +19,11 @@
 //     binades below the largest, which round to the bf16 subnormal grid with
 //     an error below 2^-134);
 //   * up to 32 candidates (one 32-row block per head): the Gram comes from the
-//     tensor cores. A CTA stacks its four heads' rows into one 128 x 128 bf16
-//     operand, one thread issues G = Y Y^T (tcgen05.mma, fp32 accumulators in
-//     128 TMEM columns) and each warp reads its head's 32 x 32 diagonal block,
-//     one Gram row per lane. The products are exact; the accumulation order
+//     tensor cores. The warps of a persistent CTA write their heads' rows into
+//     one 128 x 128 bf16 operand; each warp multiplies it by its own 32 rows
+//     (tcgen05.mma, M = 128, N = 32, fp32 accumulators in its 32 of the CTA's
+//     128 TMEM columns) and reads rows 32 w.. of the result, its head's Gram,
+//     one row per lane. The products are exact; the accumulation order
 //     and rounding are the hardware's, so the bound used assumes only fp32
 //     precision at each of the 127 additions with any rounding direction:
 //     |G32 - G| <= 127 * 2^-23 * sum_k |y_ik y_jk| <= 1.52e-5 ||y_i|| ||y_j||
@@ -44,13 +45,18 @@
 //     final when the float32 minimum beats every other candidate by more than
 //     twice its error bound - then the float64 values order the same way;
 //   * otherwise the float64 values of the close candidates are computed
-//     exactly as defined above and compared, ties going to the lowest index.
+//     exactly as defined above and compared, ties going to the lowest index;
+//     a candidate's running maximum is taken over the picks whose float32
+//     cosine lies within twice the bound of its float32 maximum only (every
+//     other pick's float64 cosine is below that maximum's).
 // The exact G_ij uses 64-bit integer arithmetic on the bf16 significands when
 // both vectors' exponents span <= 20 binades (128 products then sum below
 // 2^63), otherwise a 544-bit fixed-point accumulator over the whole bf16
-// product range; either way it is rounded once to nearest even. The per-row
-// data the exact path needs (exponent range, exact G_ii) is computed only when
-// a head meets its first close call.
+// product range; either way it is rounded once to nearest even, and a whole
+// warp evaluates one dot product (four elements per lane, exact 64-bit sums
+// added across the warp) where a decision waits on it. The per-row data the
+// exact path needs (exponent range, exact G_ii) is made when a close call
+// first needs the row.
 #include <atomic>
 #include <climits>
 
