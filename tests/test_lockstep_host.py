@@ -133,3 +133,25 @@ def test_check_unit_adopts_a_tie_band_choice():
     assert ok, rep.failures
     assert rep.kept_adopted == 1
     assert uo.pos == other
+
+
+def _drop_scores(i, res):
+    for r in res.values():
+        r.scores = None
+
+
+@pytest.mark.parametrize("plant", [None, _flip_k, _swap_kept, _change_trace])
+def test_worker_without_kept_scores(plant):
+    """With no scores kept (the handle as the throughput run configures it)
+    the keep set, the compaction and the FPS state are still compared: a
+    correct run passes and each planted mistake is still caught."""
+    def both(i, res):
+        if plant is not None:
+            plant(i, res)
+        _drop_scores(i, res)
+    rep = run_worker(library_stand_in(W, 11, UNITS, plant=both))
+    if plant is None:
+        assert not rep.failures, rep.failures
+        assert rep.units_checked == len(UNITS) * rep.evictions
+    else:
+        assert rep.failures, f"{plant.__name__} went unnoticed without scores"
