@@ -13,11 +13,18 @@
 // zero), a_i is summed left to right in j order and then divided by N. Every
 // pick this kernel makes is the pick that arithmetic makes, bit for bit, but
 // float64 runs only where it can change the answer:
-//   * each row is scaled by a power of two that brings its largest component
-//     into [1, 4), or above 2^-7 for a row of bf16 subnormals, and kept in
-//     shared memory as bf16 (exact, apart from components more than 126
-//     binades below the largest, which round to the bf16 subnormal grid with
-//     an error below 2^-134);
+//   * rows are kept in shared memory as bf16. A batch of rows whose every
+//     8-component piece is zero or has its largest magnitude in
+//     [2^-40, 2^21) is kept as loaded: each nonzero row's largest component
+//     then lies in that range, products stay below 2^44 and sums below 2^51,
+//     and the at most 255 products or partial sums flushed below 2^-126 move
+//     G_ij by less than 2^-118, under 2^-38 of ||y_i|| ||y_j|| >= 2^-80. Any other row is scaled
+//     by a power of two that brings its largest component into [1, 4), or
+//     above 2^-7 for a row of bf16 subnormals (exact, apart from components
+//     more than 126 binades below the largest, which round to the bf16
+//     subnormal grid with an error below 2^-134). Cosines do not depend on
+//     the scale; when every row is held as loaded, the kept rows are written
+//     back from shared memory;
 //   * up to 32 candidates (one 32-row block per head): the Gram comes from the
 //     tensor cores. The warps of a persistent CTA write their heads' rows into
 //     one 128 x 128 bf16 operand; each warp multiplies it by its own 32 rows
@@ -35,7 +42,8 @@
 //     (even and odd k) of 64 bf16 products each (exact, or below 2^-149 off
 //     where a product underflows), added once, so its error is at most
 //     gamma_64 * ||y_i|| ||y_j|| (3.8e-6 relative) plus < 2^-123 from the
-//     subnormal roundings, against ||y_i|| >= 2^-7 for every nonzero row;
+//     subnormal roundings, against ||y_i|| >= 2^-7 for every nonzero scaled
+//     row (2^-40 for one held as loaded);
 //   * c_ij = (G32_ij * r_i) * r_j with r_i = rsqrtf(G32_ii) (2 ulp, on a
 //     diagonal within 1.52e-5 relative) is then within 3.2e-5 of the float64
 //     cosine (8.5e-6 for the float32 Gram); the filters use kCosErr = 4e-5;
@@ -76,6 +84,8 @@ constexpr int kYStride = kD + 8;      // bf16 row stride (272 bytes): 16-byte al
 constexpr float kCosErr = 4e-5f;      // |c32 - cos64| bound used by the filters
 constexpr float kMeanErr = 4.5e-5f;   // |a32 - a64| bound used by the filters
 constexpr int kGramCols = 128;        // TMEM columns of the tensor-core Gram (4 heads x 32)
+constexpr uint32_t kRawHi = 148u << 7;  // bf16 magnitude bits of 2^21
+constexpr uint32_t kRawLo = 87u << 7;   // bf16 magnitude bits of 2^-40
 constexpr float kInfF = __builtin_huge_valf();
 
 // Per-warp shared memory for NT = 32 * NH candidate slots.
@@ -88,7 +98,7 @@ struct WarpSmem {
   static constexpr size_t kMisc = (size_t)NT * 8 * 2 + (size_t)NT * 4 * 5 + 64 * 4;
   static constexpr size_t kBytes = ((kY + kC + kMisc) + 15) / 16 * 16;
 
-  __nv_bfloat16* y;  // [NT][kYStride] rows scaled by a power of two, bf16 (exact, see the header)
+  __nv_bfloat16* y;  // [NT][kYStride] rows as loaded or scaled by a power of two, bf16 (see the header)
   float* c;       // [NT][NT + 1]   Gram, then cosines
   double* diag;   // [NT] exact G_ii rounded to float64 (close calls only)
   double* v64;    // [NT] exact values of a close call
@@ -219,9 +229,11 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta<NH>, NH == 1 ? 4 : 8) fps_ke
     return i < nb ? bq + i * 16 : rq + ((P.ring_first + i - nb) % P.n_rq) * 16;
   };
   int8_t* trace = P.trace + head * m;
+  bool raw_rows = n > m;  // every candidate row sits in shared memory exactly as loaded
 
   if (n > m) {
-    // ---- rows -> float32, each scaled so its largest component lies in [1, 4)
+    // ---- rows -> bf16 in shared memory, as loaded or each scaled so its
+    // largest component lies in [1, 4)
     // lanes 0-15 take one row, lanes 16-31 the next; padding rows are zero.
     // A batch of rows is loaded before any is processed (one memory latency
     // per batch instead of one per row pair).
@@ -236,24 +248,43 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta<NH>, NH == 1 ? 4 : 8) fps_ke
         const int r = r0 + 2 * bi + (lane >> 4);
         vb[bi] = r < n ? __ldg(row(r) + part) : make_uint4(0, 0, 0, 0);
       }
+      // a batch whose every 8-component piece is zero or has its largest
+      // magnitude in [2^-40, 2^21) is kept as loaded (then every row's
+      // largest component lies there too)
+      bool in_range = true;
+#pragma unroll
+      for (int bi = 0; bi < kLoadBatch; ++bi) {
+        uint32_t mx = 0;
+        const uint32_t w[4] = {vb[bi].x, vb[bi].y, vb[bi].z, vb[bi].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t x = w[q] & 0x7FFF7FFFu;  // bf16 magnitudes order as integers
+          mx = max(mx, max(x & 0xFFFFu, x >> 16));
+        }
+        in_range &= mx < kRawHi && (mx >= kRawLo || mx == 0u);
+      }
+      const bool raw = __all_sync(kFull, in_range);
+      raw_rows &= raw;
 #pragma unroll
       for (int bi = 0; bi < kLoadBatch; ++bi) {
         const int r = r0 + 2 * bi + (lane >> 4);
         const uint32_t w[4] = {vb[bi].x, vb[bi].y, vb[bi].z, vb[bi].w};
-        uint32_t e = 0;
+        uint32_t o[4] = {w[0], w[1], w[2], w[3]};
+        if (!raw) {
+          uint32_t e = 0;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) e = max(e, max((w[q] >> 7) & 0xFFu, (w[q] >> 23) & 0xFFu));
+          for (int q = 0; q < 4; ++q) e = max(e, max((w[q] >> 7) & 0xFFu, (w[q] >> 23) & 0xFFu));
 #pragma unroll
-        for (int off = 1; off < 16; off <<= 1) e = max(e, __shfl_xor_sync(kFull, e, off));
-        bad |= e == 0xFFu;
-        const float scale = __int_as_float(max(254 - (int)e, 1) << 23);  // 2^(127 - e)
-        uint32_t o[4];
+          for (int off = 1; off < 16; off <<= 1) e = max(e, __shfl_xor_sync(kFull, e, off));
+          bad |= e == 0xFFu;
+          const float scale = __int_as_float(max(254 - (int)e, 1) << 23);  // 2^(127 - e)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float lo = __fmul_rn(__uint_as_float(w[q] << 16), scale);
-          const float hi = __fmul_rn(__uint_as_float(w[q] & 0xFFFF0000u), scale);
-          o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-                 ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+          for (int q = 0; q < 4; ++q) {
+            const float lo = __fmul_rn(__uint_as_float(w[q] << 16), scale);
+            const float hi = __fmul_rn(__uint_as_float(w[q] & 0xFFFF0000u), scale);
+            o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+          }
         }
         if constexpr (NH == 1)  // SWIZZLE_128B K-major: 64-column slabs of 128-byte rows
           *reinterpret_cast<uint4*>(opnd + (part >> 3) * kSlabBytes + (32 * warp + r) * 128 +
@@ -351,9 +382,15 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta<NH>, NH == 1 ? 4 : 8) fps_ke
     // ---- cosines, row i by lane i (and i + 32), with the row sums for the means
     float a[NH];
     if constexpr (NH == 1) {
-      float gd = 0.f;  // the diagonal entry of this lane's row
+      // the diagonal entry of this lane's row, by selects in inline PTX: the
+      // same chain in C++ is recognised as gr[lane] and moves the row to
+      // local memory, a round trip that stalled every head
+      float gd = 0.f;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) gd = q == lane ? gr[q] : gd;
+      for (int q = 0; q < 32; ++q)
+        asm("{\n\t.reg .pred p;\n\tsetp.eq.s32 p, %2, %3;\n\tselp.f32 %0, %1, %0, p;\n\t}"
+            : "+f"(gd)
+            : "f"(gr[q]), "r"(q), "r"(lane));
       const float ri = gd > 0.f ? rsqrtf(gd) : 0.f;
       float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
@@ -501,29 +538,44 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta<NH>, NH == 1 ? 4 : 8) fps_ke
   __syncwarp();
 
   {
-    // ---- kept rows back into the beacon buffer; every source row is read
-    // before any is overwritten (m <= 31 rows of 16 uint4), through shared
-    // memory: NH == 1 this warp's operand rows (its product is done; the
-    // other warps' products only read them into rows of D nobody reads),
-    // NH == 2 the cosines
+    // ---- kept rows back into the beacon buffer (m <= 31 rows of 16 uint4).
+    // Rows held in shared memory as loaded are copied from there; otherwise
+    // every source row is read again and staged before any is overwritten:
+    // NH == 1 in this warp's operand rows (its product is done; the other
+    // warps' products only read them into rows of D nobody reads), NH == 2 in
+    // the cosines
     const int kept = n < m ? n : m;
-    auto stage = [&](int idx) -> uint4* {
-      if constexpr (NH == 1)
-        return reinterpret_cast<uint4*>(opnd + (idx >> 8) * kSlabBytes + 32 * warp * 128) + (idx & 255);
-      else
-        return reinterpret_cast<uint4*>(sm.c) + idx;
-    };
+    if (raw_rows) {
 #pragma unroll 4
-    for (int q = 0; q < 16; ++q) {
-      const int idx = lane + 32 * q;
-      if (idx < kept * 16 && BKV_IN_RANGE(sm.keep_src[idx >> 4] >= 0 && sm.keep_src[idx >> 4] < n, P.status))
-        *stage(idx) = row(sm.keep_src[idx >> 4])[idx & 15];
-    }
-    __syncwarp();
+      for (int q = 0; q < 16; ++q) {
+        const int idx = lane + 32 * q, src = sm.keep_src[idx >> 4], part = idx & 15;
+        if (idx < kept * 16 && BKV_IN_RANGE(src >= 0 && src < n, P.status)) {
+          if constexpr (NH == 1)
+            bq[idx] = *reinterpret_cast<const uint4*>(opnd + (part >> 3) * kSlabBytes + (32 * warp + src) * 128 +
+                                                      (((part & 7) ^ (src & 7)) << 4));
+          else
+            bq[idx] = *reinterpret_cast<const uint4*>(sm.y + src * kYStride + part * 8);
+        }
+      }
+    } else {
+      auto stage = [&](int idx) -> uint4* {
+        if constexpr (NH == 1)
+          return reinterpret_cast<uint4*>(opnd + (idx >> 8) * kSlabBytes + 32 * warp * 128) + (idx & 255);
+        else
+          return reinterpret_cast<uint4*>(sm.c) + idx;
+      };
 #pragma unroll 4
-    for (int q = 0; q < 16; ++q) {
-      const int idx = lane + 32 * q;
-      if (idx < kept * 16) bq[idx] = *stage(idx);
+      for (int q = 0; q < 16; ++q) {
+        const int idx = lane + 32 * q;
+        if (idx < kept * 16 && BKV_IN_RANGE(sm.keep_src[idx >> 4] >= 0 && sm.keep_src[idx >> 4] < n, P.status))
+          *stage(idx) = row(sm.keep_src[idx >> 4])[idx & 15];
+      }
+      __syncwarp();
+#pragma unroll 4
+      for (int q = 0; q < 16; ++q) {
+        const int idx = lane + 32 * q;
+        if (idx < kept * 16) bq[idx] = *stage(idx);
+      }
     }
   }
   __syncwarp();  // the next head reuses this warp's rows and cosines

@@ -457,6 +457,30 @@ def test_fps_wide_exponents_zero_rows_duplicates():
     assert_clean(rep)
 
 
+EDGE_SCALES = [-42, -41, -40, -39, 18, 19, 20, 21, 90, -110]
+
+
+def edge_magnitude_queries(t, q):
+    """Scales whole query rows by 2^s around the limits of the range FPS uses
+    rows as loaded in ([2^-40, 2^21) for the largest component of every
+    8-element piece), next to ordinary rows of the same head; one row per
+    step gets a piece of nonzero components all below 2^-40."""
+    out = q.clone()
+    s = EDGE_SCALES[t % len(EDGE_SCALES)]
+    out[..., 0, :] = (q[..., 0, :].float() * 2.0 ** s).to(q.dtype)
+    out[..., 1, :] = (q[..., 1, :].float() * 2.0 ** EDGE_SCALES[(t // 3) % len(EDGE_SCALES)]).to(q.dtype)
+    if t % 4 == 1:
+        piece = 8 * (t % 16)
+        out[..., 2, piece:piece + 8] = (q[..., 2, piece:piece + 8].float() * 2.0 ** -60).to(q.dtype)
+    return out
+
+
+def test_fps_rows_at_the_raw_range_edges():
+    w = TINY.with_(steps=300)
+    rep = run_lockstep(w, seed=5, query_hook=edge_magnitude_queries)
+    assert_clean(rep)
+
+
 def test_step_order_and_cache_length_are_validated():
     from kv_cache_eviction_head_gb300 import bkv
     w = TINY
