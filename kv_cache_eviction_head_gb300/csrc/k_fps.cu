@@ -235,9 +235,10 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta<NH>, NH == 1 ? 4 : 8) fps_ke
     // ---- rows -> bf16 in shared memory, as loaded or each scaled so its
     // largest component lies in [1, 4)
     // lanes 0-15 take one row, lanes 16-31 the next; padding rows are zero.
-    // A batch of rows is loaded before any is processed (one memory latency
-    // per batch instead of one per row pair).
-    constexpr int kLoadBatch = 8;
+    // A batch of rows is loaded before any is processed: all 32 rows at once
+    // for up to 32 candidates (one memory latency per head), 16 at a time for
+    // up to 64; the rows were prefetched into L2 during the warp's previous head.
+    constexpr int kLoadBatch = NH == 1 ? 16 : 8;
     bool bad = false;
     const int part = lane & 15;
 #pragma unroll 1
@@ -294,6 +295,11 @@ __global__ void __launch_bounds__(32 * kHeadsPerCta<NH>, NH == 1 ? 4 : 8) fps_ke
       }
     }
     if (__any_sync(kFull, bad) && lane == 0) latch(P.status, BKV_ERR_NONFINITE);
+    // this warp's next head: its candidate rows into L2 while this one computes
+    if (lane == 0 && head + stride < P.heads_total) {
+      if (nb > 0) bulk_prefetch_l2(P.bq + (head + stride) * P.fps_cap * 16, (uint32_t)nb * (kD * 2));
+      bulk_prefetch_l2(P.rq + (head + stride) * P.n_rq * 16, (uint32_t)P.n_rq * (kD * 2));
+    }
     __syncwarp();
 
     // ---- tensor-core Gram (NH == 1): this warp's 32 rows against the CTA's
