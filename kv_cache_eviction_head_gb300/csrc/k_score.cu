@@ -281,8 +281,10 @@ __device__ uint32_t select_keep(const float* sc, int L, int prefix, int recent, 
 }
 
 // Miscellaneous shared memory: control word [0, 64), dropped-slot bitmask
-// [64, 1088) (L <= 8192), copier chunk descriptors [1536, 1664).
-constexpr int kMiscBytes = 1664;
+// [64, 1088) (L <= 8192), copier chunk descriptors [1536, 1664), the copier's
+// own copy of the dropped-slot bitmask [1664, 2688) and its per-word prefix
+// counts [2688, 3712).
+constexpr int kMiscBytes = 3712;
 constexpr int kChunkRows = 32;                   // rows per compaction chunk
 constexpr int kChunkBytes = kChunkRows * kD * 2;  // 8 KB
 constexpr int kPfChunks = 16;                     // L2 prefetch lead of the copier in windows (few chunk buffers only)
@@ -627,7 +629,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
       // the chunk buffers form S sets of RW, one set per round, with the loads
       // of the next S - 1 rounds in flight. Lane i always uses buffer i of a
       // set, so its own bulk groups tell when its buffer is free again. A
-      // round's stores start once every load of the round has landed.
+      // round's stores start once every load of the round has landed. A
+      // window finds its runs and their shifts from the copier's own bitmask
+      // of the unit's dropped slots and per-word prefix counts, with bit
+      // operations instead of searches of the drop list.
       //
       // Order-free compaction: the k-th dropped slot below the budget (a hole)
       // receives the k-th kept slot at or above the budget. Sources and
@@ -767,6 +772,30 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
             ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
           } else if (!ofree) {
             const int first = D > 0 ? dl[0] + 1 : L;  // lowest source row that moves
+            // this unit's dropped slots as a bitmask with per-word prefix
+            // counts, so that a window finds its runs with bit operations (the
+            // selector's own mask already belongs to the next unit)
+            uint32_t* cbits = reinterpret_cast<uint32_t*>(smem + lay.misc + 1664);  // [ceil(L/32)]
+            int* cpre = reinterpret_cast<int*>(smem + lay.misc + 2688);             // drops in words < w
+            const int words = (L + 31) / 32;
+            for (int w = lane; w < words; w += 32) cbits[w] = 0u;
+            __syncwarp();
+            for (int i = lane; i < D; i += 32)
+              if (BKV_IN_RANGE(dl[i] >= 0 && dl[i] < L, P.status)) atomicOr(&cbits[dl[i] >> 5], 1u << (dl[i] & 31));
+            __syncwarp();
+            for (int w0 = 0, base = 0; w0 < words; w0 += 32) {
+              const int w = w0 + lane;
+              const int c = w < words ? __popc(cbits[w]) : 0;
+              int x = c;
+#pragma unroll
+              for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(kFull, x, off);
+                if (lane >= off) x += y;
+              }
+              if (w < words) cpre[w] = base + x - c;
+              base += __shfl_sync(kFull, x, 31);
+            }
+            __syncwarp();
             const int W = (L - first + kChunkRows - 1) / kChunkRows;  // windows per tensor
             const int nch = D > 0 ? 2 * W : 0;                        // K windows, then V windows
             const int nrounds = (nch + RW - 1) / RW;
@@ -824,16 +853,22 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_kernel(const __grid_
                 int s0, n;
                 window(j, dst, s0, n);
                 const uint32_t buf = smem_u32(cst + (size_t)(set * RW + lane) * kChunkBytes);
-                const int end = s0 + n;
-                int r = drops_below(dl, s0), seg = s0;
-                for (;;) {
-                  const int stop = r < D && dl[r] < end ? dl[r] : end;
-                  if (stop > seg && BKV_IN_RANGE(seg - r >= 0 && stop - r <= P.budget, P.status))
-                    bulk_store(dst + (size_t)(seg - r) * (kD * 2), buf + (uint32_t)(seg - s0) * (kD * 2),
-                               (uint32_t)(stop - seg) * (kD * 2), stream);
-                  if (stop == end) break;
-                  seg = stop + 1;
-                  ++r;
+                // bit i of dm: slot s0 + i dropped; kept runs are the runs of
+                // ones in keep, each moving down by the drops below its start
+                const int w0 = s0 >> 5, sh = s0 & 31;
+                const uint32_t lo = cbits[w0], hi = w0 + 1 < words ? cbits[w0 + 1] : 0u;
+                const uint32_t dm = sh ? (lo >> sh) | (hi << (32 - sh)) : lo;
+                const int r = cpre[w0] + __popc(lo & ((1u << sh) - 1u));  // drops below s0
+                uint32_t keep = ~dm & (n < 32 ? (1u << n) - 1u : ~0u);
+                while (keep) {
+                  const int a = __ffs(keep) - 1;
+                  const uint32_t gap = ~keep & (~0u << a);
+                  const int b = gap ? __ffs(gap) - 1 : 32;
+                  const int d0 = s0 + a - (r + __popc(dm & ((1u << a) - 1u)));
+                  if (BKV_IN_RANGE(d0 >= 0 && d0 + (b - a) <= P.budget, P.status))
+                    bulk_store(dst + (size_t)d0 * (kD * 2), buf + (uint32_t)a * (kD * 2), (uint32_t)(b - a) * (kD * 2),
+                               stream);
+                  keep = b < 32 ? keep & (~0u << b) : 0u;
                 }
               }
               bulk_commit();
